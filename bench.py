@@ -1,0 +1,466 @@
+"""Benchmark: paged-decode attention HBM GB/s and mixed-step tokens/s on GB300.
+
+One step = one pass of the decode hot path over the decode batch of 64
+sequences (32 query / 8 KV heads, head_dim 128, bf16, contexts uniform in
+[512, 4096], tables from a shuffled pool of 20,000 blocks): the KV write of the
+64 new tokens, then decode attention over the paged cache (block-table gather
+fused). ``value`` is the step's algorithmic HBM bytes (every cached K/V byte
+read once, q read, output written, new tokens read and written, tables read)
+divided by the device time per step; inputs (613 MB of K/V) exceed the 129 MB
+L2, so nothing is flushed between steps.
+
+The mixed step (budget 2048: 128 decode tokens + 4 prefill chunks of
+512/512/512/384 from 32,768-token prompts, 64/8 heads) is measured after the
+timed region and reported under ``mixed_step`` in attention tokens/s.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores. Under torchrun each rank runs its own replica
+(weak scaling, no data-path collective); rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# DRAM bytes (read + write) of one pa_decode call on the decode batch, from an
+# ncu capture (profiles/decode_b64_bf16.md), valid for the kernel source whose
+# sha256 prefix is given; null once the source changes.
+NCU_DECODE_TRAFFIC = {"bytes": None, "src_sha": None}
+
+
+def _src_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def peaks() -> dict:
+    try:
+        with open(MEASURED_PEAKS) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def step_bytes(w) -> dict:
+    """Algorithmic HBM bytes of one decode step (KV write + decode)."""
+    elt = w.k_pool.element_size()
+    tok = w.num_kv_heads * w.head_dim * elt
+    kv_read = int(w.context_lens.to("cpu").long().sum()) * 2 * tok
+    q_out = 2 * w.q.numel() * elt
+    nblk = int(((w.context_lens.long() + 15) // 16).sum())
+    tables = nblk * 4 + w.num_seqs * 4
+    write = 2 * 2 * w.num_tokens * tok + w.num_tokens * 8 if w.slot_mapping is not None else 0
+    decode = kv_read + q_out + tables
+    return {"decode": decode, "write": write, "step": decode + write, "kv_read": kv_read}
+
+
+def mixed_work(w) -> dict:
+    """Algorithmic work of a mixed step: decode KV bytes, prefill causal FLOPs
+    (QK^T and PV over the unmasked keys of every prefill row)."""
+    cu = w.cu_q_lens.tolist()
+    ctx = w.context_lens.tolist()
+    elt = w.k_pool.element_size()
+    tok = w.num_kv_heads * w.head_dim * elt
+    dec_bytes, flops, pf_kv = 0, 0, 0
+    for s in range(w.num_seqs):
+        ql = cu[s + 1] - cu[s]
+        if ql == 1:
+            dec_bytes += ctx[s] * 2 * tok
+        elif ql > 1:
+            off = ctx[s] - ql
+            keys = ql * off + ql * (ql + 1) // 2
+            flops += 4 * w.num_q_heads * w.head_dim * keys
+            pf_kv += ctx[s] * 2 * tok
+    return {"decode_bytes": dec_bytes, "prefill_flops": flops, "prefill_kv_bytes": pf_kv}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def run_gpu(args, rank: int, world: int) -> dict | None:
+    import torch
+    import paged_kv_cache_176_gb300 as pa
+    from paged_kv_cache_176_gb300 import workloads as W
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    pa.abi.load()
+    w = W.decode_b64(seed=args.seed)
+    nb = step_bytes(w)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        kp, vp = w.k_pool.to(dev), w.v_pool.to(dev)
+        q, bt, cl = w.q.to(dev), w.block_tables.to(dev), w.context_lens.to(dev)
+        kn, vn, sm = w.k_new.to(dev), w.v_new.to(dev), w.slot_mapping.to(dev)
+        out = torch.empty_like(q)
+        ws = torch.empty(pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.head_dim,
+                                                     w.max_blocks_per_seq),
+                         dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)
+    launches_per_step = 3  # KV write, decode, split-K merge
+
+    def step():
+        pa.pa_reshape_and_cache(kp, vp, kn, vn, sm, stream=stream)
+        pa.pa_decode(out, q, kp, vp, bt, cl, w.scale, workspace=ws, stream=stream)
+
+    # decode-call timing (dominant kernel pair), measured on its own stream
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    n_ev = min(args.steps, 200)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_ev)]
+    for a, b in ev:
+        pa.pa_reshape_and_cache(kp, vp, kn, vn, sm, stream=stream)
+        a.record(stream)
+        pa.pa_decode(out, q, kp, vp, bt, cl, w.scale, workspace=ws, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    decode_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    # timed region: exactly K steps
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+        tdist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index).start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    if dist:
+        tm = torch.tensor([ms], dtype=torch.float64, device=dev)
+        tdist.all_reduce(tm, op=tdist.ReduceOp.MAX)
+        ms = float(tm.item())
+
+    # end to end through the public API with host buffers
+    pin = {k: t.pin_memory() for k, t in (("q", w.q), ("k_new", w.k_new), ("v_new", w.v_new),
+                                            ("slot", w.slot_mapping), ("bt", w.block_tables),
+                                            ("cl", w.context_lens))}
+    host_out = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(50, min(args.steps, 2000))
+
+    def e2e_step():
+        q.copy_(pin["q"], non_blocking=True)
+        kn.copy_(pin["k_new"], non_blocking=True)
+        vn.copy_(pin["v_new"], non_blocking=True)
+        sm.copy_(pin["slot"], non_blocking=True)
+        bt.copy_(pin["bt"], non_blocking=True)
+        cl.copy_(pin["cl"], non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        wall0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        wall = (time.perf_counter() - wall0) / e2e_steps * 1e3
+    e2e_ms = max(e0.elapsed_time(e1) / e2e_steps, wall)
+
+    # mixed step (secondary measurement)
+    mixed = None
+    if not args.skip_mixed:
+        mixed = run_mixed(args, dev, stream)
+
+    pk = peaks()
+    decode_gbs = nb["decode"] / (decode_ms * 1e-3) / 1e9
+    src = os.path.join(ROOT, "paged_kv_cache_176_gb300", "csrc", "decode.cu")
+    traffic = None
+    if NCU_DECODE_TRAFFIC["bytes"] and NCU_DECODE_TRAFFIC["src_sha"] == _src_sha(src):
+        traffic = NCU_DECODE_TRAFFIC["bytes"]
+    value = world * nb["step"] / (ms * 1e-3) / 1e9
+    res = {
+        "metric": "paged-decode attention HBM GB/s (% of peak) and mixed-step tokens/s on 1 GB300",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16-rounded; no dataset)",
+        "config": {"workload": "decode_b64_bf16: 64 seqs, ctx U[512,4096], 32/8 heads, d 128, "
+                               "block 16, pool 20000 shuffled blocks, + KV write of 64 tokens",
+                   "kv_bytes_per_step": nb["kv_read"], "algorithmic_bytes_per_step": nb["step"],
+                   "l2": "inputs 613 MB > 129 MB L2; no flush",
+                   "parallelism": f"replicas x{world}"},
+        "attention_tokens_per_s": round(world * w.num_seqs / (ms * 1e-3), 1),
+        "kv_tokens_scanned_per_s": round(world * int(w.context_lens.sum()) / (ms * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_kernel + decode_reduce_kernel)",
+                     "achieved": round(decode_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(decode_gbs / pk["hbm_gbs"], 4), "traffic": traffic,
+                     "peak_source": pk["source"], "ms_per_launch": round(decode_ms, 5),
+                     "algorithmic_bytes_per_launch": nb["decode"]},
+        "e2e": {"value": round(world * nb["step"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if mixed is not None:
+        res["mixed_step"] = mixed
+    return res
+
+
+def run_mixed(args, dev, stream) -> dict:
+    import torch
+    import paged_kv_cache_176_gb300 as pa
+    from paged_kv_cache_176_gb300 import workloads as W
+
+    w = W.mixed_step(seed=args.seed)
+    work = mixed_work(w)
+    with torch.cuda.stream(stream):
+        d = {k: getattr(w, k).to(dev) for k in ("k_pool", "v_pool", "q", "cu_q_lens",
+                                               "context_lens", "block_tables", "k_new", "v_new",
+                                               "slot_mapping")}
+        out = torch.empty_like(d["q"])
+        ws = torch.empty(pa.pa_mixed_workspace_size(w.num_seqs, w.num_tokens, w.num_q_heads,
+                                                    w.head_dim, w.max_blocks_per_seq),
+                         dtype=torch.uint8, device=dev)
+
+    def step():
+        pa.pa_mixed_step(out, d["q"], d["cu_q_lens"], d["context_lens"], d["block_tables"],
+                         d["k_pool"], d["v_pool"], w.scale, w.token_budget, k_new=d["k_new"],
+                         v_new=d["v_new"], slot_mapping=d["slot_mapping"], workspace=ws,
+                         stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    step()
+    torch.cuda.synchronize(dev)
+    one = time.perf_counter() - t0
+    n = max(3, min(args.mixed_steps, int(10.0 / max(one, 1e-4))))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / n
+    pk = peaks()
+    tflops = work["prefill_flops"] / (ms * 1e-3) / 1e12
+    return {
+        "workload": "mixed_step_bf16: budget 2048 = 128 decode (ctx U[1024,8192]) + prefill "
+                    "512/512/512/384 at 512-aligned offsets of 32768-token prompts; 64/8 heads, d 128",
+        "steps": n,
+        "ms_per_step": round(ms, 4),
+        "tokens_per_s": round(w.num_tokens / (ms * 1e-3), 1),
+        "prefill_tflops_step": round(tflops, 2),
+        "tensor_frac_step": round(tflops / pk["bf16_tflops_sustained"], 4),
+        "decode_gbs_step": round(work["decode_bytes"] / (ms * 1e-3) / 1e9, 1),
+        "prefill_flops": work["prefill_flops"],
+        "decode_bytes": work["decode_bytes"],
+    }
+
+
+# ------------------------------------------------------------------ oracle arm
+
+
+def run_oracle_sample(seed: int, budget_s: float) -> dict:
+    """The fp64 oracle, as it stands, on a bounded sample of the decode
+    workload: the KV write plus attention for as many sequences as fit the
+    time budget (sequence order of the workload). Returns GB/s in the same
+    algorithmic-byte accounting as the GPU arm."""
+    import numpy as np
+    import torch
+    import oracle
+    from paged_kv_cache_176_gb300 import workloads as W
+
+    w = W.decode_b64(seed=seed)
+    lib = oracle.load()
+    kp, vp = w.k_pool.clone(), w.v_pool.clone()
+    cores = os.cpu_count() or 1
+    t_write0 = time.perf_counter()
+    oracle.reshape_and_cache(kp, vp, w.k_new, w.v_new, w.slot_mapping, lib=lib)
+    t_write = time.perf_counter() - t_write0
+    done, t_att = 0, 0.0
+    byte_count = 0
+    nb_all = step_bytes(w)
+    tok_bytes = 2 * w.num_kv_heads * w.head_dim * w.k_pool.element_size()
+    mask = np.zeros(w.num_seqs, dtype=np.uint8)
+    while done < w.num_seqs and t_att < budget_s:
+        k = min(w.num_seqs - done, max(1, cores // 2))
+        m = mask.copy()
+        m[done:done + k] = 1
+        t0 = time.perf_counter()
+        oracle.paged_attention(w.q, kp, vp, w.cu_q_lens, w.context_lens, w.block_tables, w.scale,
+                               row_mask=m, num_threads=cores, lib=lib)
+        t_att += time.perf_counter() - t0
+        byte_count += int(w.context_lens[done:done + k].long().sum()) * tok_bytes
+        done += k
+    q_etc = (nb_all["decode"] - nb_all["kv_read"]) * done / w.num_seqs
+    total_bytes = byte_count + q_etc + nb_all["write"]
+    secs = t_att + t_write
+    return {"value": total_bytes / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"KV write of all {w.num_tokens} tokens + attention of the first {done} of "
+                      f"{w.num_seqs} sequences ({byte_count / 1e6:.0f} MB of K/V) in {secs:.1f} s",
+            "seconds": round(secs, 2), "seqs": done}
+
+
+def run_reference(args, rank: int, world: int) -> dict | None:
+    if rank != 0:
+        return None
+    base = None
+    times = []
+    for _ in range(args.warmup):
+        run_oracle_sample(args.seed, budget_s=2.0)
+    for _ in range(args.steps):
+        r = run_oracle_sample(args.seed, budget_s=args.ref_budget_s)
+        times.append(r)
+        base = r
+    v = statistics.median(r["value"] for r in times)
+    ms = statistics.median(r["seconds"] for r in times) * 1e3
+    return {
+        "impl": "reference",
+        "metric": "paged-decode attention HBM GB/s (% of peak) and mixed-step tokens/s on 1 GB300",
+        "value": round(v, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode_b64_bf16 (bounded sample per step)"},
+        "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": base["cores"],
+                         "kind": "oracle", "sample": base["sample"]},
+        "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--mixed-steps", type=int, default=200)
+    ap.add_argument("--skip-mixed", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-budget-s", type=float, default=8.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as tdist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if args.impl != "reference":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group(backend)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_gpu(args, rank, world)
+        if res is not None and rank == 0 and not args.skip_cpu_baseline:
+            res["cpu_baseline"] = run_oracle_sample(args.seed, args.cpu_budget_s)
+            res["cpu_baseline"] = {k: (round(v, 3) if isinstance(v, float) else v)
+                                   for k, v in res["cpu_baseline"].items()}
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.barrier()
+        tdist.destroy_process_group()
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

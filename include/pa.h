@@ -1,0 +1,179 @@
+/*
+ * pa.h -- C ABI of libpa: attention over a paged KV cache on one GB300 (sm_103a).
+ *
+ * The KV cache is a pool of fixed-size physical blocks; every sequence owns a
+ * block table mapping its logical blocks to physical block IDs ("vLLM serving
+ * internals", section "PagedAttention as a virtual memory system"; the page
+ * table of "Inference engine core techniques", section 1.2). Attention gathers
+ * each sequence's K/V through its table (K_r = gather(K_pool, table_r), the
+ * gather figure of "C13 L2 serving: continuous batching and PagedAttention").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers marked "device" are CUDA device pointers owned by the caller; the
+ *    library allocates no memory and keeps no state between calls.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream). PA_OK means "validated and enqueued".
+ *  - Host-side validation looks only at scalars and pointer values; on any
+ *    failure the call returns a negative pa_status and enqueues nothing.
+ *  - Data-dependent errors (a table entry outside the pool, a context longer
+ *    than the table, q_len > context, a slot outside the pool) are found on
+ *    the device: the kernel ORs a PA_STATUS_* bit into *d_status (when
+ *    d_status is not NULL), skips the bad access and writes zeros for the
+ *    affected output rows. Nothing traps.
+ *  - Layouts are row-major and contiguous:
+ *      K/V pool     [num_blocks, block_size, num_kv_heads, head_dim]
+ *      q, out       [num_tokens, num_q_heads, head_dim]
+ *      k_new, v_new [num_tokens, num_kv_heads, head_dim]
+ *      block_tables int32 [num_seqs, max_blocks_per_seq]
+ *    Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *  - Supported: block_size 16; head_dim 64, 128 or 256; num_q_heads a multiple
+ *    of num_kv_heads with a ratio of 1, 2, 4 or 8; num_kv_heads <= 8 for
+ *    decode; dtype PA_F32 or PA_BF16. Accumulation is fp32; outputs are
+ *    written in the input dtype (bf16 with round-to-nearest-even).
+ *  - Every device pointer must be 16-byte aligned.
+ *  - Calls are re-entrant; concurrent calls must not share a workspace.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_EINVAL = -1,        /* null/misaligned pointer, negative or inconsistent size */
+  PA_EUNSUPPORTED = -2,  /* block size, head_dim, head ratio or dtype not built */
+  PA_EWORKSPACE = -3,    /* workspace NULL or smaller than the size query */
+  PA_EBUDGET = -4,       /* num_tokens > token_budget */
+  PA_ECUDA = -5          /* a kernel launch failed (the CUDA error is cleared) */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits ORed into *d_status by the kernels. */
+#define PA_STATUS_BAD_BLOCK 1u   /* block table entry outside [0, num_blocks) */
+#define PA_STATUS_BAD_LENGTH 2u  /* context <= 0, context > max_blocks_per_seq * block_size,
+                                    q_len > context, or inconsistent cu_q_lens */
+#define PA_STATUS_BAD_SLOT 4u    /* slot_mapping entry >= num_blocks * block_size */
+#define PA_STATUS_TIMEOUT 8u     /* a bounded wait on an asynchronous copy gave up */
+
+/* The KV pool of one layer: borrowed device memory, never freed by libpa. */
+typedef struct {
+  void* k;              /* device, [num_blocks, block_size, num_kv_heads, head_dim] */
+  void* v;              /* device, same shape as k */
+  int64_t num_blocks;   /* N_blk */
+  int32_t block_size;   /* b, tokens per block: 16 */
+  int32_t num_kv_heads; /* Hkv */
+  int32_t head_dim;     /* d */
+  int32_t dtype;        /* pa_dtype */
+} pa_kv_pool;
+
+/* Human-readable text for a pa_status value (static storage). */
+PA_API const char* pa_strerror(int status);
+
+/* ABI version: (major << 16) | minor. */
+PA_API int pa_version(void);
+
+/*
+ * KV write ("reshape and cache"): for every token t with slot_mapping[t] >= 0,
+ * copy k_new[t] and v_new[t] into the pool at physical block slot / block_size,
+ * offset slot % block_size. slot_mapping[t] == -1 marks a padding token and is
+ * skipped. The copy is byte-exact for either dtype. The cache grows this way,
+ * block by block ("Chunked Prefill" page, section on how chunked prefill works).
+ *
+ *  pool          K/V pool (written in place)
+ *  k_new, v_new  device, [num_tokens, num_kv_heads, head_dim], pool dtype
+ *  slot_mapping  device int64 [num_tokens]
+ *  num_tokens    >= 0 (0 enqueues nothing)
+ *  Any head_dim works here as long as a token row (num_kv_heads * head_dim
+ *  elements) is a multiple of 16 bytes.
+ *  d_status      device int32 or NULL; PA_STATUS_BAD_SLOT for slots past the pool
+ */
+PA_API int pa_reshape_and_cache(const pa_kv_pool* pool, const void* k_new, const void* v_new,
+                         const int64_t* slot_mapping, int num_tokens, int* d_status,
+                         void* stream);
+
+/* Bytes of workspace pa_decode needs for these sizes (0 on invalid sizes). */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                int max_blocks_per_seq);
+
+/*
+ * Decode attention: one query token per sequence attends to the whole cached
+ * context of that sequence (decode reads the entire cache each step: "Chunked
+ * Prefill" page, section on prefill, decode and generation stalls). The block
+ * loop follows the paged_attn pseudo-kernel of "Inference engine core
+ * techniques", section 1.4: per page, look up the physical page, read its K/V,
+ * accumulate with an online softmax. Long contexts are split over several
+ * CTAs and the partial (max, sum, accumulator) triples are merged by a second
+ * kernel; the split depends only on the context lengths, so results are
+ * bit-identical under any relabelling of physical blocks.
+ *
+ *  out           device, [num_seqs, num_q_heads, head_dim], pool dtype
+ *  q             device, [num_seqs, num_q_heads, head_dim], pool dtype
+ *  block_tables  device int32 [num_seqs, max_blocks_per_seq]
+ *  context_lens  device int32 [num_seqs]; tokens attended (>= 1)
+ *  scale         softmax scale applied to q.k (e.g. 1/sqrt(head_dim))
+ *  workspace     device, >= pa_decode_workspace_size(...) bytes, 16-byte aligned
+ */
+PA_API int pa_decode(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+              int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
+              const int32_t* context_lens, float scale, void* workspace,
+              size_t workspace_bytes, int* d_status, void* stream);
+
+/*
+ * Tuning knob: the number of persistent CTAs the decode kernel runs (0, the
+ * default, means one per SM of the current device; values above 1024 are
+ * clamped). It applies to later pa_decode / pa_mixed_step calls from any
+ * thread. Returns the previous value. Results do not depend on it beyond
+ * floating-point summation order.
+ */
+PA_API int pa_set_decode_ctas(int num_ctas);
+
+/* Bytes of workspace pa_mixed_step needs for these sizes (0 on invalid sizes). */
+PA_API size_t pa_mixed_workspace_size(int num_seqs, int num_tokens, int num_q_heads, int head_dim,
+                               int max_blocks_per_seq);
+
+/*
+ * Mixed step: one call for a batch of decode tokens and prefill chunks under a
+ * token budget (the step of iteration-level scheduling with chunked prefill:
+ * "Chunked Prefill" page, section on how it works; "vLLM serving internals",
+ * scheduler loop, "one fused GPU call"). Sequence s owns query rows
+ * cu_q_lens[s] .. cu_q_lens[s+1]-1; its q_len = cu_q_lens[s+1] - cu_q_lens[s]
+ * rows are the LAST q_len positions of its context_lens[s] tokens, so row i
+ * sits at absolute position context_lens[s] - q_len + i and attends keys
+ * 0 .. that position (causal over absolute positions, as in the glossary
+ * page's chunked-prefill example). q_len == 1 rows take the decode kernel;
+ * q_len > 1 rows take the prefill kernel (tcgen05 tensor cores for bf16). The
+ * result equals one-pass causal prefill for any chunk split.
+ *
+ *  cu_q_lens     device int32 [num_seqs + 1], cu_q_lens[0] = 0, non-decreasing,
+ *                cu_q_lens[num_seqs] = num_tokens
+ *  context_lens  device int32 [num_seqs]; includes this step's tokens
+ *  token_budget  num_tokens must not exceed it (PA_EBUDGET otherwise)
+ *  k_new, v_new, slot_mapping
+ *                NULL, or the step's new K/V ([num_tokens, Hkv, d]) and slots:
+ *                when given, the KV write runs first, on the same stream
+ *  workspace     device, >= pa_mixed_workspace_size(...) bytes
+ */
+PA_API int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_t* cu_q_lens,
+                  int num_seqs, int num_tokens, int num_q_heads, const int32_t* context_lens,
+                  const int32_t* block_tables, int max_blocks_per_seq, float scale,
+                  int token_budget, const void* k_new, const void* v_new,
+                  const int64_t* slot_mapping, void* workspace, size_t workspace_bytes,
+                  int* d_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

@@ -1,0 +1,214 @@
+"""ctypes binding of libpa (include/pa.h). Argument marshalling only.
+
+Every function here has the name of the C entry point it calls and passes
+PyTorch tensors' device pointers, sizes and the current CUDA stream through.
+All computation happens in libpa's CUDA kernels; there is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+PA_OK = 0
+PA_EINVAL = -1
+PA_EUNSUPPORTED = -2
+PA_EWORKSPACE = -3
+PA_EBUDGET = -4
+PA_ECUDA = -5
+PA_F32 = 0
+PA_BF16 = 1
+PA_STATUS_BAD_BLOCK = 1
+PA_STATUS_BAD_LENGTH = 2
+PA_STATUS_BAD_SLOT = 4
+PA_STATUS_TIMEOUT = 8
+
+
+class pa_kv_pool(ctypes.Structure):
+    _fields_ = [
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("num_blocks", ctypes.c_int64),
+        ("block_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+    ]
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status} ({pa_strerror(status)})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpa.so (built by ``paged_kv_cache_176_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m paged_kv_cache_176_gb300.build`")
+        lib = ctypes.CDLL(path)
+        P, I, I64, SZ, F = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                            ctypes.c_float)
+        PP = ctypes.POINTER(pa_kv_pool)
+        lib.pa_strerror.restype = ctypes.c_char_p
+        lib.pa_strerror.argtypes = [I]
+        lib.pa_version.restype = I
+        lib.pa_version.argtypes = []
+        lib.pa_reshape_and_cache.restype = I
+        lib.pa_reshape_and_cache.argtypes = [PP, P, P, P, I, P, P]
+        lib.pa_decode_workspace_size.restype = SZ
+        lib.pa_decode_workspace_size.argtypes = [I, I, I, I]
+        lib.pa_decode.restype = I
+        lib.pa_decode.argtypes = [PP, P, P, I, I, P, I, P, F, P, SZ, P, P]
+        lib.pa_mixed_workspace_size.restype = SZ
+        lib.pa_mixed_workspace_size.argtypes = [I, I, I, I, I]
+        lib.pa_mixed_step.restype = I
+        lib.pa_mixed_step.argtypes = [PP, P, P, P, I, I, I, P, P, I, F, I, P, P, P, P, SZ, P, P]
+        lib.pa_set_decode_ctas.restype = I
+        lib.pa_set_decode_ctas.argtypes = [I]
+        _lib = lib
+        return lib
+
+
+def pa_strerror(status: int) -> str:
+    return load().pa_strerror(int(status)).decode()
+
+
+def pa_version() -> int:
+    return int(load().pa_version())
+
+
+def pa_set_decode_ctas(n: int) -> int:
+    """Number of persistent decode CTAs (0: one per SM). Returns the old value."""
+    return int(load().pa_set_decode_ctas(int(n)))
+
+
+# ----------------------------------------------------------------- helpers
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    if t.dtype == torch.float32:
+        return PA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libpa takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libpa takes contiguous tensors")
+    return t.data_ptr()
+
+
+def make_pool(k_pool: torch.Tensor, v_pool: torch.Tensor) -> pa_kv_pool:
+    if k_pool.shape != v_pool.shape or k_pool.dtype != v_pool.dtype or k_pool.dim() != 4:
+        raise ValueError("k_pool/v_pool must both be [num_blocks, block_size, Hkv, d]")
+    nb, b, hkv, d = k_pool.shape
+    return pa_kv_pool(_ptr(k_pool), _ptr(v_pool), nb, b, hkv, d, _dtype_code(k_pool))
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != PA_OK:
+        raise PagedAttentionError(fn, rc)
+
+
+# ----------------------------------------------------------------- entry points
+
+
+def pa_reshape_and_cache(k_pool, v_pool, k_new, v_new, slot_mapping, d_status=None,
+                         stream=None) -> None:
+    """KV write: scatter k_new/v_new [T, Hkv, d] into the pools at slot_mapping."""
+    lib = load()
+    pool = make_pool(k_pool, v_pool)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    T = int(slot_mapping.shape[0])
+    if T and (k_new.shape[0] != T or v_new.shape[0] != T):
+        raise ValueError("k_new/v_new/slot_mapping disagree on num_tokens")
+    _check("pa_reshape_and_cache",
+           lib.pa_reshape_and_cache(ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                    T, _ptr(d_status), _stream(stream)))
+
+
+def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int,
+                             max_blocks_per_seq: int) -> int:
+    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_blocks_per_seq))
+
+
+def pa_mixed_workspace_size(num_seqs: int, num_tokens: int, num_q_heads: int, head_dim: int,
+                            max_blocks_per_seq: int) -> int:
+    return int(load().pa_mixed_workspace_size(num_seqs, num_tokens, num_q_heads, head_dim,
+                                              max_blocks_per_seq))
+
+
+def _workspace(nbytes: int, device, workspace) -> torch.Tensor:
+    if workspace is not None:
+        return workspace
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale: float, workspace=None,
+              d_status=None, stream=None):
+    """Decode attention, q/out [S, Hq, d]. Returns out."""
+    lib = load()
+    pool = make_pool(k_pool, v_pool)
+    S, hq, d = q.shape
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    mb = int(block_tables.shape[1])
+    ws = _workspace(pa_decode_workspace_size(S, hq, d, mb), q.device, workspace)
+    _check("pa_decode",
+           lib.pa_decode(ctypes.byref(pool), _ptr(out), _ptr(q), S, hq, _ptr(block_tables), mb,
+                         _ptr(context_lens), float(scale), _ptr(ws), ws.numel() * ws.element_size(),
+                         _ptr(d_status), _stream(stream)))
+    return out
+
+
+def pa_mixed_step(out, q, cu_q_lens, context_lens, block_tables, k_pool, v_pool, scale: float,
+                  token_budget: int, k_new=None, v_new=None, slot_mapping=None, workspace=None,
+                  d_status=None, stream=None):
+    """Mixed decode + prefill-chunk step, q/out [T, Hq, d]. Returns out."""
+    lib = load()
+    pool = make_pool(k_pool, v_pool)
+    T, hq, d = q.shape
+    S = int(context_lens.shape[0])
+    if (cu_q_lens.dtype != torch.int32 or block_tables.dtype != torch.int32
+            or context_lens.dtype != torch.int32):
+        raise TypeError("cu_q_lens, block_tables and context_lens must be int32")
+    mb = int(block_tables.shape[1])
+    ws = _workspace(pa_mixed_workspace_size(S, T, hq, d, mb), q.device, workspace)
+    _check("pa_mixed_step",
+           lib.pa_mixed_step(ctypes.byref(pool), _ptr(out), _ptr(q), _ptr(cu_q_lens), S, T, hq,
+                             _ptr(context_lens), _ptr(block_tables), mb, float(scale),
+                             int(token_budget), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                             _ptr(ws), ws.numel() * ws.element_size(), _ptr(d_status),
+                             _stream(stream)))
+    return out

@@ -1,0 +1,262 @@
+// api.cu -- the C ABI declared in include/pa.h: host-side validation of the
+// scalar arguments, workspace size queries, and dispatch to the kernels.
+// Host validation never dereferences a device pointer; data-dependent checks
+// happen in the kernels (see pa.h).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+int device_sm_count() {
+  // cached per device: the attribute query is cheap but not free
+  static std::mutex mu;
+  static std::vector<int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+std::atomic<int> g_decode_ctas{0};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Pool checks shared by every entry point (the KV write needs no more).
+int check_pool_storage(const pa_kv_pool* pool) {
+  if (pool == nullptr || pool->k == nullptr || pool->v == nullptr) return PA_EINVAL;
+  if (!aligned16(pool->k) || !aligned16(pool->v)) return PA_EINVAL;
+  if (pool->num_blocks <= 0 || pool->num_kv_heads <= 0 || pool->head_dim <= 0) return PA_EINVAL;
+  if (pool->block_size != 16) return PA_EUNSUPPORTED;
+  if (pool->dtype != PA_F32 && pool->dtype != PA_BF16) return PA_EUNSUPPORTED;
+  const int64_t elt = pool->dtype == PA_BF16 ? 2 : 4;
+  if ((pool->num_kv_heads * pool->head_dim * elt) % 16 != 0) return PA_EUNSUPPORTED;
+  return PA_OK;
+}
+
+// Attention kernels are built for head_dim 64, 128 and 256.
+int check_pool(const pa_kv_pool* pool) {
+  int rc = check_pool_storage(pool);
+  if (rc != PA_OK) return rc;
+  if (pool->head_dim != 64 && pool->head_dim != 128 && pool->head_dim != 256) return PA_EUNSUPPORTED;
+  return PA_OK;
+}
+
+PoolView view(const pa_kv_pool* pool) {
+  PoolView v;
+  v.k = pool->k;
+  v.v = pool->v;
+  v.num_blocks = pool->num_blocks;
+  v.num_kv_heads = pool->num_kv_heads;
+  v.head_dim = pool->head_dim;
+  v.dtype = pool->dtype;
+  return v;
+}
+
+int check_heads(const pa_kv_pool* pool, int num_q_heads) {
+  if (num_q_heads <= 0) return PA_EINVAL;
+  if (num_q_heads % pool->num_kv_heads != 0) return PA_EINVAL;
+  const int group = num_q_heads / pool->num_kv_heads;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return PA_EUNSUPPORTED;
+  return PA_OK;
+}
+
+int to_status(cudaError_t err) {
+  if (err == cudaSuccess) return PA_OK;
+  cudaGetLastError();  // clear a sticky launch error so the caller's next launch is clean
+  return PA_ECUDA;
+}
+
+int validate_kv_write(const pa_kv_pool* pool, const void* k_new, const void* v_new,
+                      const int64_t* slot_mapping, int num_tokens) {
+  int rc = check_pool_storage(pool);
+  if (rc != PA_OK) return rc;
+  if (num_tokens < 0) return PA_EINVAL;
+  if (num_tokens == 0) return PA_OK;
+  if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return PA_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PA_EINVAL;
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_strerror(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_EINVAL: return "invalid argument (null or misaligned pointer, bad size)";
+    case PA_EUNSUPPORTED: return "unsupported configuration (block size, head_dim, head ratio or dtype)";
+    case PA_EWORKSPACE: return "workspace missing or too small";
+    case PA_EBUDGET: return "num_tokens exceeds token_budget";
+    case PA_ECUDA: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+int pa_version(void) { return (1 << 16) | 0; }
+
+int pa_set_decode_ctas(int num_ctas) {
+  if (num_ctas < 0) num_ctas = 0;
+  return g_decode_ctas.exchange(num_ctas);
+}
+
+int pa_reshape_and_cache(const pa_kv_pool* pool, const void* k_new, const void* v_new,
+                         const int64_t* slot_mapping, int num_tokens, int* d_status,
+                         void* stream) {
+  int rc = validate_kv_write(pool, k_new, v_new, slot_mapping, num_tokens);
+  if (rc != PA_OK || num_tokens == 0) return rc;
+  KvWriteArgs a;
+  a.pool = view(pool);
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.d_status = d_status;
+  return to_status(launch_kv_write(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                int max_blocks_per_seq) {
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0) return 0;
+  return decode_workspace_bytes(num_seqs, num_q_heads, head_dim);
+}
+
+int pa_decode(const pa_kv_pool* pool, void* out, const void* q, int num_seqs, int num_q_heads,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              float scale, void* workspace, size_t workspace_bytes, int* d_status, void* stream) {
+  int rc = check_pool(pool);
+  if (rc != PA_OK) return rc;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0) return PA_EINVAL;
+  rc = check_heads(pool, num_q_heads);
+  if (rc != PA_OK) return rc;
+  if (!decode_supported(pool->dtype, pool->head_dim, num_q_heads / pool->num_kv_heads,
+                        pool->num_kv_heads))
+    return PA_EUNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (out == nullptr || q == nullptr || block_tables == nullptr || context_lens == nullptr)
+    return PA_EINVAL;
+  if (!aligned16(out) || !aligned16(q)) return PA_EINVAL;
+  const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, pool->head_dim,
+                                               max_blocks_per_seq);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PA_EWORKSPACE;
+  DecodeArgs a = {};
+  a.pool = view(pool);
+  a.out = out;
+  a.q = q;
+  a.cu_q_lens = nullptr;
+  a.num_seqs = num_seqs;
+  a.num_rows = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.scale = scale;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.d_status = d_status;
+  a.grid_override = g_decode_ctas.load();
+  return to_status(launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t pa_mixed_workspace_size(int num_seqs, int num_tokens, int num_q_heads, int head_dim,
+                               int max_blocks_per_seq) {
+  if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || head_dim <= 0 ||
+      max_blocks_per_seq <= 0)
+    return 0;
+  return decode_workspace_bytes(num_seqs, num_q_heads, head_dim);
+}
+
+int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_t* cu_q_lens,
+                  int num_seqs, int num_tokens, int num_q_heads, const int32_t* context_lens,
+                  const int32_t* block_tables, int max_blocks_per_seq, float scale,
+                  int token_budget, const void* k_new, const void* v_new,
+                  const int64_t* slot_mapping, void* workspace, size_t workspace_bytes,
+                  int* d_status, void* stream) {
+  int rc = check_pool(pool);
+  if (rc != PA_OK) return rc;
+  if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq <= 0) return PA_EINVAL;
+  rc = check_heads(pool, num_q_heads);
+  if (rc != PA_OK) return rc;
+  if (num_tokens > token_budget) return PA_EBUDGET;
+  if (!decode_supported(pool->dtype, pool->head_dim, num_q_heads / pool->num_kv_heads,
+                        pool->num_kv_heads) ||
+      !prefill_supported(pool->dtype, pool->head_dim, num_q_heads / pool->num_kv_heads))
+    return PA_EUNSUPPORTED;
+  const bool write = k_new != nullptr || v_new != nullptr || slot_mapping != nullptr;
+  if (write) {
+    rc = validate_kv_write(pool, k_new, v_new, slot_mapping, num_tokens);
+    if (rc != PA_OK) return rc;
+  }
+  if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+  if (out == nullptr || q == nullptr || cu_q_lens == nullptr || block_tables == nullptr ||
+      context_lens == nullptr)
+    return PA_EINVAL;
+  if (!aligned16(out) || !aligned16(q)) return PA_EINVAL;
+  const size_t need = pa_mixed_workspace_size(num_seqs, num_tokens, num_q_heads, pool->head_dim,
+                                              max_blocks_per_seq);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PA_EWORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (write) {
+    KvWriteArgs w;
+    w.pool = view(pool);
+    w.k_new = k_new;
+    w.v_new = v_new;
+    w.slot_mapping = slot_mapping;
+    w.num_tokens = num_tokens;
+    w.d_status = d_status;
+    rc = to_status(launch_kv_write(w, st));
+    if (rc != PA_OK) return rc;
+  }
+  PrefillArgs pf;
+  pf.pool = view(pool);
+  pf.out = out;
+  pf.q = q;
+  pf.cu_q_lens = cu_q_lens;
+  pf.num_seqs = num_seqs;
+  pf.num_tokens = num_tokens;
+  pf.num_q_heads = num_q_heads;
+  pf.block_tables = block_tables;
+  pf.max_blocks_per_seq = max_blocks_per_seq;
+  pf.context_lens = context_lens;
+  pf.scale = scale;
+  pf.d_status = d_status;
+  rc = to_status(launch_prefill(pf, st));
+  if (rc != PA_OK) return rc;
+  DecodeArgs a = {};
+  a.pool = view(pool);
+  a.out = out;
+  a.q = q;
+  a.cu_q_lens = cu_q_lens;
+  a.num_seqs = num_seqs;
+  a.num_rows = num_tokens;
+  a.num_q_heads = num_q_heads;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.scale = scale;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.d_status = d_status;
+  a.grid_override = g_decode_ctas.load();
+  return to_status(launch_decode(a, st));
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// pa_internal.h -- launch parameters shared between the C-ABI layer (api.cu)
+// and the kernel translation units. Host code only; no device code here.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+struct PoolView {
+  void* k;
+  void* v;
+  int64_t num_blocks;
+  int num_kv_heads;
+  int head_dim;
+  int dtype;
+};
+
+// ---- KV write
+struct KvWriteArgs {
+  PoolView pool;
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+  int num_tokens;
+  int* d_status;
+};
+cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream);
+
+// ---- decode (q_len == 1 rows)
+struct DecodeArgs {
+  PoolView pool;
+  void* out;                 // rows indexed by seq (or by cu_q_lens[s] when given)
+  const void* q;
+  const int32_t* cu_q_lens;  // NULL: row of sequence s is s; else cu_q_lens[s], and
+                             // only sequences with q_len == 1 are processed
+  int num_seqs;
+  int num_rows;              // rows of q/out (num_seqs, or num_tokens of a mixed step)
+  int num_q_heads;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  float scale;
+  void* workspace;
+  size_t workspace_bytes;
+  int* d_status;
+  int grid_override;         // > 0: number of persistent CTAs (tuning / tests)
+};
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim);
+bool decode_supported(int dtype, int head_dim, int group, int num_kv_heads);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// ---- prefill chunks (q_len > 1 rows of a mixed step)
+struct PrefillArgs {
+  PoolView pool;
+  void* out;
+  const void* q;
+  const int32_t* cu_q_lens;
+  int num_seqs;
+  int num_tokens;
+  int num_q_heads;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  float scale;
+  int* d_status;
+};
+bool prefill_supported(int dtype, int head_dim, int group);
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace pa

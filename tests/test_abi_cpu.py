@@ -1,0 +1,111 @@
+"""The C-ABI library loads, exports every declared symbol, and its host-side
+validation rejects bad arguments before any CUDA call (runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_176_gb300 import abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return abi.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_strerror(lib):
+    assert abi.pa_version() >> 16 == 1
+    for code in (0, -1, -2, -3, -4, -5):
+        assert abi.pa_strerror(code)
+    assert abi.pa_strerror(-99) == "unknown status"
+
+
+FAKE = 0x10000  # aligned, never dereferenced by host validation
+
+
+def pool(**kw):
+    p = dict(k=FAKE, v=FAKE, num_blocks=32, block_size=16, num_kv_heads=2, head_dim=64, dtype=0)
+    p.update(kw)
+    return abi.pa_kv_pool(p["k"], p["v"], p["num_blocks"], p["block_size"], p["num_kv_heads"],
+                          p["head_dim"], p["dtype"])
+
+
+def decode(lib, pl, q=FAKE, out=FAKE, hq=8, S=4, mb=8, ws=FAKE, ws_bytes=1 << 40):
+    return lib.pa_decode(ctypes.byref(pl), out, q, S, hq, FAKE, mb, FAKE, 0.125, ws, ws_bytes,
+                         None, None)
+
+
+def test_decode_validation(lib):
+    assert decode(lib, pool(k=None)) == abi.PA_EINVAL
+    assert decode(lib, pool(v=FAKE + 4)) == abi.PA_EINVAL          # misaligned
+    assert decode(lib, pool(block_size=8)) == abi.PA_EUNSUPPORTED
+    assert decode(lib, pool(head_dim=96)) == abi.PA_EUNSUPPORTED
+    assert decode(lib, pool(dtype=7)) == abi.PA_EUNSUPPORTED
+    assert decode(lib, pool(), hq=6) == abi.PA_EUNSUPPORTED        # group 3
+    assert decode(lib, pool(), hq=7) == abi.PA_EINVAL              # not a multiple
+    assert decode(lib, pool(num_kv_heads=16), hq=16) == abi.PA_EUNSUPPORTED
+    assert decode(lib, pool(), q=None) == abi.PA_EINVAL
+    assert decode(lib, pool(), out=FAKE + 8) == abi.PA_EINVAL
+    assert decode(lib, pool(), ws=None) == abi.PA_EWORKSPACE
+    assert decode(lib, pool(), ws_bytes=16) == abi.PA_EWORKSPACE
+    assert decode(lib, pool(), S=-1) == abi.PA_EINVAL
+    assert decode(lib, pool(), S=0) == abi.PA_OK                   # nothing to do
+
+
+def test_workspace_queries(lib):
+    assert abi.pa_decode_workspace_size(-1, 8, 64, 8) == 0
+    a = abi.pa_decode_workspace_size(4, 8, 64, 8)
+    b = abi.pa_decode_workspace_size(64, 32, 128, 256)
+    assert 0 < a < b
+    assert abi.pa_mixed_workspace_size(4, 10, 8, 64, 8) >= a
+
+
+def test_mixed_and_write_validation(lib):
+    pl = pool()
+    rc = lib.pa_mixed_step(ctypes.byref(pl), FAKE, FAKE, FAKE, 2, 100, 8, FAKE, FAKE, 8, 0.1, 64,
+                           None, None, None, FAKE, 1 << 40, None, None)
+    assert rc == abi.PA_EBUDGET
+    rc = lib.pa_mixed_step(ctypes.byref(pl), FAKE, FAKE, FAKE, 2, 10, 8, FAKE, FAKE, 8, 0.1, 64,
+                           FAKE, None, FAKE, FAKE, 1 << 40, None, None)  # v_new missing
+    assert rc == abi.PA_EINVAL
+    rc = lib.pa_mixed_step(ctypes.byref(pl), FAKE, FAKE, None, 2, 10, 8, FAKE, FAKE, 8, 0.1, 64,
+                           None, None, None, FAKE, 1 << 40, None, None)
+    assert rc == abi.PA_EINVAL
+    rc = lib.pa_mixed_step(ctypes.byref(pl), FAKE, FAKE, FAKE, 2, 10, 8, FAKE, FAKE, 8, 0.1, 64,
+                           None, None, None, FAKE, 16, None, None)
+    assert rc == abi.PA_EWORKSPACE
+    assert lib.pa_reshape_and_cache(ctypes.byref(pl), FAKE, FAKE, FAKE, -1, None, None) == abi.PA_EINVAL
+    assert lib.pa_reshape_and_cache(ctypes.byref(pl), None, FAKE, FAKE, 3, None, None) == abi.PA_EINVAL
+    assert lib.pa_reshape_and_cache(ctypes.byref(pl), FAKE + 2, FAKE, FAKE, 3, None, None) == abi.PA_EINVAL
+    assert lib.pa_reshape_and_cache(ctypes.byref(pl), FAKE, FAKE, FAKE, 0, None, None) == abi.PA_OK
+
+
+def test_decode_cta_knob(lib):
+    old = abi.pa_set_decode_ctas(7)
+    assert abi.pa_set_decode_ctas(old) == 7
+
+
+def test_binding_rejects_host_tensors():
+    import torch
+    k = torch.zeros(4, 16, 2, 64)
+    with pytest.raises(ValueError):
+        abi.make_pool(k, k)

@@ -1,0 +1,258 @@
+"""GPU parity: the CUDA path, called through the C-ABI binding, against the
+fp64 oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_pins
+import paged_kv_cache_176_gb300 as pa
+from paged_kv_cache_176_gb300 import workloads as W
+from parity import compare, oracle_out, run_decode, run_mixed, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _default_ctas():
+    old = pa.pa_set_decode_ctas(0)
+    yield
+    pa.pa_set_decode_ctas(old)
+
+
+def _bytes(t: torch.Tensor) -> np.ndarray:
+    t = t.contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        t = t.view(torch.int16)
+    return t.numpy().view(np.uint8)
+
+
+# ------------------------------------------------------------------ KV write
+
+
+@pytest.mark.parametrize("make", [W.tiny_decode_f32, lambda: oracle_pins._mixed_small(8)],
+                         ids=["f32", "bf16"])
+def test_kv_write_bit_exact(make):
+    w = make()
+    if w.slot_mapping is None:  # give the fp32 case new tokens too
+        w = W.paged_workload("w", 3, [17, 40, 64, 100], [5, 1, 16, 33], 8, 2, 64, 32,
+                             torch.float32, write_new=True)
+    sm = w.slot_mapping.clone()
+    sm[::7] = -1  # padding tokens are skipped
+    db = to_device(w)
+    pa.pa_reshape_and_cache(db.k_pool, db.v_pool, db.k_new, db.v_new, sm.cuda(), d_status=db.status)
+    torch.cuda.synchronize()
+    kp, vp = w.k_pool.clone(), w.v_pool.clone()
+    oracle.reshape_and_cache(kp, vp, w.k_new, w.v_new, sm)
+    assert np.array_equal(_bytes(db.k_pool), _bytes(kp))
+    assert np.array_equal(_bytes(db.v_pool), _bytes(vp))
+    assert int(db.status.item()) == 0
+
+
+def test_kv_write_full_config_bit_exact():
+    w = W.decode_b64()
+    db = to_device(w)
+    pa.pa_reshape_and_cache(db.k_pool, db.v_pool, db.k_new, db.v_new, db.slot_mapping)
+    torch.cuda.synchronize()
+    kp, vp = w.k_pool.clone(), w.v_pool.clone()
+    oracle.reshape_and_cache(kp, vp, w.k_new, w.v_new, w.slot_mapping)
+    assert np.array_equal(_bytes(db.k_pool), _bytes(kp))
+    assert np.array_equal(_bytes(db.v_pool), _bytes(vp))
+
+
+def test_kv_write_bad_slot_flags_and_skips():
+    w = oracle_pins._mixed_small(9)
+    sm = w.slot_mapping.clone()
+    sm[0] = w.num_blocks * 16  # one past the pool
+    db = to_device(w)
+    before = _bytes(db.k_pool).copy()
+    pa.pa_reshape_and_cache(db.k_pool, db.v_pool, db.k_new, db.v_new, sm.cuda(), d_status=db.status)
+    torch.cuda.synchronize()
+    assert int(db.status.item()) & pa.abi.PA_STATUS_BAD_SLOT
+    kp = w.k_pool.clone()
+    sm_ok = sm.clone()
+    sm_ok[0] = -1
+    oracle.reshape_and_cache(kp, w.v_pool.clone(), w.k_new, w.v_new, sm_ok)
+    assert np.array_equal(_bytes(db.k_pool), _bytes(kp))
+    assert not np.array_equal(before, _bytes(db.k_pool))
+
+
+# ------------------------------------------------------------------ decode
+
+
+def test_decode_tiny_f32():
+    w = W.tiny_decode_f32()
+    out, db = run_decode(w)
+    info = compare(out, oracle_out(w), torch.float32)
+    assert int(db.status.item()) == 0, info
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 64, 1024])
+def test_decode_split_counts(ctas):
+    """Every CTA count gives the same result within tolerance, including a
+    count far above the number of blocks (empty CTAs, many partials)."""
+    w = W.paged_workload("split", 5, [1, 15, 16, 17, 33, 100, 257, 600], [1] * 8, 16, 4, 128, 200,
+                         torch.bfloat16, write_new=True)
+    pa.pa_set_decode_ctas(ctas)
+    out, db = run_decode(w)
+    compare(out, oracle_out(w), torch.bfloat16)
+    assert int(db.status.item()) == 0
+
+
+@pytest.mark.parametrize("d,hq,hkv,dtype", [
+    (64, 8, 8, torch.bfloat16), (64, 16, 2, torch.float32), (128, 8, 1, torch.bfloat16),
+    (128, 16, 4, torch.float32), (256, 16, 8, torch.bfloat16), (256, 8, 1, torch.float32),
+    (128, 64, 8, torch.bfloat16), (256, 32, 4, torch.bfloat16),
+])
+def test_decode_shapes(d, hq, hkv, dtype):
+    w = W.paged_workload("shape", 11, [3, 16, 31, 200, 513], [1] * 5, hq, hkv, d, 128, dtype,
+                         write_new=True)
+    for ctas in (0, 5):
+        pa.pa_set_decode_ctas(ctas)
+        out, _ = run_decode(w)
+        compare(out, oracle_out(w), dtype)
+
+
+def test_decode_b64_full():
+    w = W.decode_b64()
+    out, db = run_decode(w)
+    info = compare(out, oracle_out(w), torch.bfloat16)
+    assert int(db.status.item()) == 0, info
+
+
+def test_wide_gqa_full():
+    w = W.wide_gqa_decode()
+    out, db = run_decode(w)
+    compare(out, oracle_out(w), torch.bfloat16)
+    assert int(db.status.item()) == 0
+
+
+def test_shared_prefix_full_and_cow_bit_identical():
+    ws = W.shared_prefix_decode()
+    out_s, _ = run_decode(ws)
+    compare(out_s, oracle_out(ws), torch.bfloat16)
+    wp = W.shared_prefix_decode(private=True)
+    out_p, _ = run_decode(wp)
+    assert torch.equal(out_s, out_p)  # copy-on-write sharing == private copies, bit for bit
+
+
+def test_decode_permutation_bit_identical():
+    w = W.decode_b64(num_seqs=16, num_blocks=1200, ctx_range=(100, 1000))
+    out_a, _ = run_decode(w)
+    out_b, _ = run_decode(oracle_pins.permute_pool(w, 4))
+    assert torch.equal(out_a, out_b)
+
+
+def test_decode_bad_block_and_length_zeroed():
+    w = W.paged_workload("bad", 2, [40, 40, 40], [1, 1, 1], 8, 2, 64, 32, torch.float32,
+                         write_new=False)
+    bt = w.block_tables.clone()
+    bt[1, 1] = w.num_blocks + 5
+    ctx = w.context_lens.clone()
+    ctx[2] = bt.shape[1] * 16 + 1  # longer than the table
+    w2 = W.Workload(w.name, w.dtype, w.num_q_heads, w.num_kv_heads, w.head_dim, 16, w.k_pool,
+                    w.v_pool, w.q, w.cu_q_lens, ctx, bt, None, None, None, w.scale, 3)
+    out, db = run_decode(w2)
+    st = int(db.status.item())
+    assert st & pa.abi.PA_STATUS_BAD_BLOCK and st & pa.abi.PA_STATUS_BAD_LENGTH
+    assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[2]) == 0
+    good = oracle.paged_attention(w.q[:1], w.k_pool, w.v_pool, torch.tensor([0, 1], dtype=torch.int32),
+                                  w.context_lens[:1], w.block_tables[:1], w.scale)
+    compare(out[:1], good, torch.float32)
+
+
+def test_decode_empty_batch():
+    w = W.tiny_decode_f32()
+    db = to_device(w)
+    out = torch.zeros(0, w.num_q_heads, w.head_dim, device="cuda")
+    pa.pa_decode(out, db.q[:0], db.k_pool, db.v_pool, db.block_tables[:0], db.context_lens[:0],
+                 w.scale)
+
+
+# ------------------------------------------------------------------ mixed step
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_mixed_small(dtype):
+    w = oracle_pins._mixed_small(12, dtype, hq=8, hkv=2, d=64)
+    out, db = run_mixed(w)
+    compare(out, oracle_out(w), dtype)
+    assert int(db.status.item()) == 0
+
+
+def test_chunked_prefill_example_on_gpu():
+    """The glossary page's experiment through pa_mixed_step: 1000 tokens in
+    chunks of 256/256/256/232 equal one-pass causal prefill within 1e-5, and
+    both equal the oracle."""
+    r = oracle_pins.chunked_prefill_example(oracle.load())
+    torch.manual_seed(0)
+    q, k, v = torch.randn(3, 1, 8, 1000, 64).unbind(0)
+    qt = q[0].transpose(0, 1).contiguous().cuda()
+    kt = k[0].transpose(0, 1).contiguous().cuda()
+    vt = v[0].transpose(0, 1).contiguous().cuda()
+    nblk = 63
+    perm = torch.randperm(80, generator=torch.Generator().manual_seed(1))[:nblk].to(torch.int32)
+    table = perm.reshape(1, nblk).cuda()
+    pos = torch.arange(1000)
+    slots = (perm[pos // 16].to(torch.int64) * 16 + pos % 16).cuda()
+
+    def run(chunk):
+        kp = torch.full((80, 16, 8, 64), float("nan"), device="cuda")
+        vp = torch.full_like(kp, float("nan"))
+        outs = []
+        for start in range(0, 1000, chunk):
+            end = min(start + chunk, 1000)
+            o = torch.empty(end - start, 8, 64, device="cuda")
+            pa.pa_mixed_step(o, qt[start:end], torch.tensor([0, end - start], dtype=torch.int32).cuda(),
+                             torch.tensor([end], dtype=torch.int32).cuda(), table, kp, vp, 0.125,
+                             2048, k_new=kt[start:end], v_new=vt[start:end],
+                             slot_mapping=slots[start:end])
+            outs.append(o)
+        return torch.cat(outs).cpu()
+
+    chunked, one_pass = run(256), run(1000)
+    assert torch.allclose(one_pass, chunked, atol=1e-5, rtol=0)
+    compare(chunked, r["sdpa_fp64"], torch.float32)
+    compare(one_pass, r["one_pass"], torch.float32)
+
+
+def test_mixed_step_scaled_full():
+    """Config-4 structure with 4,096-token prompts, every row checked."""
+    w = W.mixed_step(num_decode=16, decode_ctx=(64, 2048), prompt_len=4096)
+    out, db = run_mixed(w)
+    compare(out, oracle_out(w), torch.bfloat16)
+    assert int(db.status.item()) == 0
+
+
+def test_mixed_step_full_sampled():
+    w = W.mixed_step()
+    out, db = run_mixed(w)
+    assert int(db.status.item()) == 0
+    nd = w.info["num_decode"]
+    rng = np.random.default_rng(0)
+    mask = np.zeros(w.num_tokens, dtype=np.uint8)
+    mask[:nd] = 1
+    cu = w.cu_q_lens.tolist()
+    for s in range(nd, w.num_seqs):
+        rows = rng.choice(np.arange(cu[s], cu[s + 1]), size=8, replace=False)
+        mask[rows] = 1
+        mask[cu[s + 1] - 1] = 1  # last row of each chunk (longest key range)
+    ref = oracle_out(w, row_mask=mask)
+    compare(out, ref, torch.bfloat16, rows=np.nonzero(mask)[0])
+
+
+def test_mixed_permutation_bit_identical():
+    w = W.mixed_step(num_decode=8, decode_ctx=(64, 1024), prompt_len=2048)
+    out_a, _ = run_mixed(w)
+    out_b, _ = run_mixed(oracle_pins.permute_pool(w, 5))
+    assert torch.equal(out_a, out_b)
+
+
+def test_mixed_budget_rejected():
+    w = oracle_pins._mixed_small(13, d=64)
+    db = to_device(w)
+    out = torch.empty_like(db.q)
+    with pytest.raises(pa.PagedAttentionError) as e:
+        pa.pa_mixed_step(out, db.q, db.cu_q_lens, db.context_lens, db.block_tables, db.k_pool,
+                         db.v_pool, w.scale, w.num_tokens - 1)
+    assert e.value.status == pa.abi.PA_EBUDGET
