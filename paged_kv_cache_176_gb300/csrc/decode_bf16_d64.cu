@@ -1,0 +1,8 @@
+// decode_bf16_d64.cu -- decode kernels for bf16 pools with head_dim 64.
+#include "decode_impl.cuh"
+
+namespace pa {
+cudaError_t decode_bf16_d64(const DecodeArgs& a, int group, cudaStream_t stream) {
+  return dispatch_decode_d<__nv_bfloat16, 64>(a, group, stream);
+}
+}  // namespace pa

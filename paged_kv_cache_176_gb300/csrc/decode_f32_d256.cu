@@ -1,0 +1,8 @@
+// decode_f32_d256.cu -- decode kernels for f32 pools with head_dim 256.
+#include "decode_impl.cuh"
+
+namespace pa {
+cudaError_t decode_f32_d256(const DecodeArgs& a, int group, cudaStream_t stream) {
+  return dispatch_decode_d<float, 256>(a, group, stream);
+}
+}  // namespace pa

@@ -1,0 +1,739 @@
+// decode_impl.cuh -- paged decode attention on sm_103a (SIMT, HBM-bound).
+// Included by one translation unit per (dtype, head_dim): decode_<dtype>_d<D>.cu.
+//
+// What it computes: for every decode sequence s and query head h (KV head
+// g = h / G), o[s,h] = softmax_p(scale * q[s,h] . K_s[p,g]) V_s[p,g] over
+// p < ctx_s, where K_s/V_s is the sequence's cache gathered through its block
+// table. The block loop is the paged_attn pseudo-kernel of "Inference engine
+// core techniques", section 1.4 (per page: look up the physical page, read
+// its K/V, accumulate with an online softmax); the gather is K_r =
+// gather(K_pool, table_r) from the "C13 L2 serving" page.
+//
+// GB300 design:
+//  * Persistent grid, one CTA per SM. The blocks of all decode sequences,
+//    concatenated in sequence order, are cut into `grid` equal contiguous
+//    ranges, one per CTA (balanced split-K: every CTA reads the same number of
+//    KV bytes whatever the context mix). A sequence inside one CTA's range is
+//    finished by that CTA; a sequence that straddles CTAs leaves one partial
+//    (max, sum, accumulator) per CTA, merged by decode_reduce_kernel. The cut
+//    depends only on the context lengths, so the result is bit-identical under
+//    any relabelling of physical blocks or sharing of blocks.
+//  * A pool block stores its 16 tokens x all KV heads contiguously, so one
+//    1-D bulk copy (cp.async.bulk) moves a whole block of K (and one of V)
+//    into shared memory: 16-byte aligned, fully coalesced. A 3-4 stage
+//    mbarrier pipeline keeps >= 2 blocks (up to 128 KB) in flight per SM. The
+//    CTA's slice of the block tables is staged in shared memory up front.
+//  * Warps are decoupled: each waits only on the stage it reads, and the last
+//    warp to finish a stage (a shared-memory counter) refills it. No CTA-wide
+//    barrier runs in the steady state.
+//  * Warp w serves KV head w % Hkv (and 1/WH of each block's tokens when a
+//    KV head has WH > 1 warps). Up to four query heads of the GQA group live
+//    in each lane's registers, so one K/V element read from shared memory
+//    feeds four FMAs; larger groups split their heads over lane groups.
+//    Lanes split a token's head_dim in 16-byte chunks; packed fp32x2 FMAs
+//    (FFMA2) do the dot products and the P.V update.
+//  * Online softmax in the log2 domain (q pre-scaled by scale*log2 e) with a
+//    lazy running max: the accumulator is rescaled only when a new score
+//    exceeds the running max by more than 8 (weights stay <= 256), decided
+//    per warp so the rescale is a uniform branch.
+//  * Tokens past the context (the tail of a last block) are never loaded and
+//    never touched, so stale or NaN slots cannot leak into the result.
+#pragma once
+#include <algorithm>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTableCache = 1024;     // block-table entries staged in shared memory
+constexpr float kRescaleThreshold = 8.0f;
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <typename T, int D, int G, int WH>
+struct Cfg {
+  static constexpr int kHkv = kWarps / WH;
+  static constexpr int kElt = sizeof(T);
+  static constexpr int kVec = 16 / kElt;             // elements per 16-byte chunk
+  static constexpr int kGL = G < 4 ? G : 4;          // query heads per lane
+  static constexpr int kHG = G / kGL;                // head groups per token
+  static constexpr int kTokPerWarp = kBlockSize / WH;  // tokens of a full block per warp
+  // lane slice: q and the accumulator hold kGL * kC floats each (<= 64), and
+  // the warp's token slots should not outnumber its tokens per block
+  static constexpr int kCq = 64 / kGL;
+  static constexpr int kCtok = D * kHG * kTokPerWarp / 32;
+  static constexpr int kC0 = kCq < kCtok ? kCq : kCtok;
+  static constexpr int kC1 = kC0 < D ? kC0 : D;
+  static constexpr int kC = kC1 > kVec ? kC1 : kVec;  // elements per lane per token
+  static constexpr int kLpt = D / kC;                 // lanes per (token, head group)
+  static constexpr int kLanesTok = kLpt * kHG;        // lanes per token
+  static constexpr int kTg = 32 / kLanesTok;          // token slots per warp
+  static constexpr int kChunks = kC / kVec;
+  static constexpr int kPairs = kC / 2;
+  static constexpr int kNt = kTokPerWarp / kTg > 0 ? kTokPerWarp / kTg : 1;
+  static constexpr int kBatch = kNt < 4 ? kNt : 4;    // tokens per softmax update per slot
+  static_assert(kC % kVec == 0, "lane slice must be whole 16-byte chunks");
+  static_assert(kLanesTok >= 1 && kLanesTok <= 32 && 32 % kLanesTok == 0, "bad lane split");
+  static_assert(G % kGL == 0, "bad head split");
+};
+
+struct SmemLayout {
+  int stages;
+  int tokens_per_unit;  // tokens of one block moved per pipeline stage (16, 8 or 4)
+  int parts;            // 16 / tokens_per_unit
+  int part_bytes;       // one K (or V) part: tokens_per_unit * Hkv * D * elt
+  int off_bars, off_done, off_flags, off_mbars, off_table, off_merge, off_prefix, total;
+};
+
+__host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline SmemLayout make_layout(int stages, int tokens_per_unit, int hkv, int d,
+                                                  int elt, int wh, int group, int num_seqs) {
+  SmemLayout L;
+  L.stages = stages;
+  L.tokens_per_unit = tokens_per_unit;
+  L.parts = kBlockSize / tokens_per_unit;
+  L.part_bytes = tokens_per_unit * hkv * d * elt;
+  const int off = stages * 2 * L.part_bytes;
+  L.off_bars = align_up(off, 16);
+  L.off_done = L.off_bars + stages * 8;
+  L.off_flags = L.off_done + stages * 4;
+  L.off_mbars = align_up(L.off_flags + stages * 4, 16);   // 2 merge mbarriers per KV head
+  L.off_table = align_up(L.off_mbars + 2 * hkv * 8, 16);
+  L.off_merge = align_up(L.off_table + kTableCache * 4, 16);
+  const int merge_bytes = (wh - 1) * hkv * group * (d + 2) * 4;
+  L.off_prefix = align_up(L.off_merge + merge_bytes, 16);
+  L.total = align_up(L.off_prefix + (num_seqs + 1) * 4, 128);
+  return L;
+}
+
+struct DecodeParams {
+  const char* k_pool;
+  const char* v_pool;
+  int64_t num_blocks;
+  int hkv;
+  int hq;
+  const void* q;
+  void* out;
+  const int32_t* cu_q_lens;
+  int num_seqs;
+  int num_rows;  // rows of q/out
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* context_lens;
+  float scale_log2;
+  int* ws_prefix;  // [num_seqs + 1]
+  float2* ws_ml;   // [slots, hq] (m, l)
+  float* ws_acc;   // [slots, hq, D]
+  int* d_status;
+  SmemLayout L;
+};
+
+// Blocks the decode kernel reads for sequence s (0 when s is not a decode
+// sequence or its lengths are invalid).
+__device__ __forceinline__ int decode_blocks(const DecodeParams& p, int s, bool* bad) {
+  int q_len = 1;
+  if (p.cu_q_lens != nullptr) {
+    q_len = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
+    if (q_len < 0 || p.cu_q_lens[s] < 0 || p.cu_q_lens[s + 1] > p.num_rows) {
+      *bad = true;  // malformed cu_q_lens: never index q/out with it
+      return 0;
+    }
+  }
+  if (q_len != 1) return 0;
+  const int ctx = p.context_lens[s];
+  if (ctx < 1 || ctx > p.max_blocks * kBlockSize) {
+    *bad = true;
+    return 0;
+  }
+  return (ctx + kBlockSize - 1) / kBlockSize;
+}
+
+__device__ __forceinline__ int query_row(const DecodeParams& p, int s) {
+  return p.cu_q_lens != nullptr ? p.cu_q_lens[s] : s;
+}
+
+// 16 bytes of T from shared memory as fp32 pairs.
+template <typename T>
+__device__ __forceinline__ void load_pairs(const T* src, float2* dst) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(src);
+  if constexpr (sizeof(T) == 2) {
+    dst[0] = bf16x2_to_float2(raw.x);
+    dst[1] = bf16x2_to_float2(raw.y);
+    dst[2] = bf16x2_to_float2(raw.z);
+    dst[3] = bf16x2_to_float2(raw.w);
+  } else {
+    dst[0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+    dst[1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
+  }
+}
+
+// Rescale factor of a partial with running max m when the merged max is mn.
+__device__ __forceinline__ float merge_factor(float m, float mn) {
+  return m == -INFINITY ? 0.f : fast_exp2(m - mn);
+}
+
+template <typename T, int D, int G, int WH>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+  using C = Cfg<T, D, G, WH>;
+  constexpr int HKV = C::kHkv;
+  extern __shared__ __align__(128) char smem[];
+  const SmemLayout& L = p.L;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
+  int* done = reinterpret_cast<int*>(smem + L.off_done);
+  int* flags = reinterpret_cast<int*>(smem + L.off_flags);
+  uint64_t* merge_full = reinterpret_cast<uint64_t*>(smem + L.off_mbars);
+  uint64_t* merge_empty = merge_full + HKV;
+  int* table = reinterpret_cast<int*>(smem + L.off_table);
+  float* merge = reinterpret_cast<float*>(smem + L.off_merge);
+  int* prefix = reinterpret_cast<int*>(smem + L.off_prefix);
+  __shared__ int warp_sums[kWarps];
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int S = p.num_seqs;
+
+  if (tid == 0) {
+    for (int i = 0; i < L.stages; ++i) {
+      mbar_init(&bars[i], 1);
+      done[i] = 0;
+    }
+    for (int i = 0; i < HKV; ++i) {
+      mbar_init(&merge_full[i], WH - 1 > 0 ? WH - 1 : 1);
+      mbar_init(&merge_empty[i], 1);
+    }
+    fence_mbar_init();
+  }
+  bool bad_len = false;
+  block_exclusive_scan<kThreads>(
+      S, [&](int s) { return decode_blocks(p, s, &bad_len); }, prefix, warp_sums);
+  if (bad_len && blockIdx.x == 0) status_or(p.d_status, PA_STATUS_BAD_LENGTH);
+
+  // Invalid decode sequences (bad lengths) get zero output rows, written once.
+  if (blockIdx.x == 0) {
+    for (int s = warp; s < S; s += kWarps) {
+      bool bad = false;
+      const bool decode_row = decode_blocks(p, s, &bad) > 0 || bad;
+      int q_len = 1;
+      if (p.cu_q_lens != nullptr) q_len = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
+      const int row = query_row(p, s);
+      if (decode_row && bad && q_len == 1 && row >= 0 && row < p.num_rows) {
+        T* o = static_cast<T*>(p.out) + static_cast<int64_t>(row) * p.hq * D;
+        for (int i = lane; i < p.hq * D; i += 32) o[i] = from_float<T>(0.f);
+      }
+    }
+    for (int i = tid; i <= S; i += kThreads) p.ws_prefix[i] = prefix[i];
+  }
+
+  const int64_t B = prefix[S];
+  const int64_t grid = gridDim.x;
+  const int64_t lo = static_cast<int64_t>(blockIdx.x) * B / grid;
+  const int64_t hi = (static_cast<int64_t>(blockIdx.x) + 1) * B / grid;
+  if (lo >= hi) return;
+
+  // stage this CTA's slice of the block tables (first kTableCache blocks)
+  const int n_cached = static_cast<int>(min(hi - lo, static_cast<int64_t>(kTableCache)));
+  for (int i = tid; i < n_cached; i += kThreads) {
+    const int s = upper_index(prefix, S, lo + i);
+    table[i] = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + (lo + i - prefix[s])];
+  }
+  __syncthreads();
+
+  const int parts = L.parts;
+  const int tpu = L.tokens_per_unit;
+  const int64_t n_units = (hi - lo) * parts;
+  constexpr int kTokenBytes = HKV * D * C::kElt;
+
+  // Issue unit u into its stage (called by one lane).
+  auto issue = [&](int64_t u) {
+    const int st = static_cast<int>(u % L.stages);
+    const int64_t blk = lo + u / parts;
+    const int part = static_cast<int>(u % parts);
+    const int s = upper_index(prefix, S, blk);
+    const int j = static_cast<int>(blk - prefix[s]);  // logical block of sequence s
+    const int ctx = p.context_lens[s];
+    const int64_t rel = blk - lo;
+    const int phys = rel < kTableCache ? table[rel]
+                                       : p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
+    const int first_tok = j * kBlockSize + part * tpu;
+    const int ntok = min(tpu, ctx - first_tok);
+    if (phys < 0 || phys >= p.num_blocks) {
+      flags[st] = -1;
+      status_or(p.d_status, PA_STATUS_BAD_BLOCK);
+      mbar_arrive(&bars[st]);
+    } else if (ntok <= 0) {
+      flags[st] = 0;
+      mbar_arrive(&bars[st]);
+    } else {
+      flags[st] = ntok;
+      const uint32_t bytes = static_cast<uint32_t>(ntok * kTokenBytes);
+      const int64_t src = (static_cast<int64_t>(phys) * kBlockSize + part * tpu) * kTokenBytes;
+      char* kdst = smem + st * 2 * L.part_bytes;
+      mbar_arrive_expect_tx(&bars[st], 2 * bytes);
+      bulk_g2s(kdst, p.k_pool + src, bytes, &bars[st]);
+      bulk_g2s(kdst + L.part_bytes, p.v_pool + src, bytes, &bars[st]);
+    }
+  };
+  if (tid == 0) {
+    for (int64_t u = 0; u < min(static_cast<int64_t>(L.stages), n_units); ++u) issue(u);
+  }
+
+  // ---------------------------------------------------------------- consumers
+  const int g = warp % HKV;     // this warp's KV head
+  const int sub = warp / HKV;   // which share of a block's tokens
+  const int tg = lane / C::kLanesTok;                  // token slot
+  const int hg = (lane / C::kLpt) % C::kHG;            // head group
+  const int kl = lane % C::kLpt;                       // chunk column
+  const int head0 = g * G + hg * C::kGL;               // first query head of this lane
+
+  float2 qf[C::kGL][C::kPairs];
+  float2 acc[C::kGL][C::kPairs];
+  float m[C::kGL], l[C::kGL];
+  int merges = 0;  // sequences merged across warps so far (mbarrier phase)
+
+  int64_t u = 0;
+  int s = upper_index(prefix, S, lo);
+  bool ok = true;
+  while (u < n_units && ok) {
+    while (prefix[s + 1] <= lo + u / parts) ++s;
+    const int64_t seq_lo = max(lo, static_cast<int64_t>(prefix[s]));
+    const int64_t seq_hi = min(hi, static_cast<int64_t>(prefix[s + 1]));
+    const int64_t seq_units = (seq_hi - seq_lo) * parts;
+    const bool whole = prefix[s] >= lo && prefix[s + 1] <= hi;
+    const int row = query_row(p, s);
+
+    // this lane's query heads, pre-scaled into the log2 domain
+    {
+      const T* qrow = static_cast<const T*>(p.q) + (static_cast<int64_t>(row) * p.hq + head0) * D;
+#pragma unroll
+      for (int h = 0; h < C::kGL; ++h) {
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          float2 pr[C::kVec / 2];
+          const uint4 raw =
+              __ldg(reinterpret_cast<const uint4*>(qrow + h * D + (kl + C::kLpt * c) * C::kVec));
+          if constexpr (sizeof(T) == 2) {
+            pr[0] = bf16x2_to_float2(raw.x);
+            pr[1] = bf16x2_to_float2(raw.y);
+            pr[2] = bf16x2_to_float2(raw.z);
+            pr[3] = bf16x2_to_float2(raw.w);
+          } else {
+            pr[0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+            pr[1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
+          }
+#pragma unroll
+          for (int i = 0; i < C::kVec / 2; ++i)
+            qf[h][c * (C::kVec / 2) + i] = make_float2(pr[i].x * p.scale_log2, pr[i].y * p.scale_log2);
+        }
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int i = 0; i < C::kPairs; ++i) acc[h][i] = make_float2(0.f, 0.f);
+      }
+    }
+    bool poisoned = false;
+
+    for (int64_t su = 0; su < seq_units; ++su, ++u) {
+      const int st = static_cast<int>(u % L.stages);
+      const uint32_t parity = static_cast<uint32_t>((u / L.stages) & 1);
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], parity));
+      if (!ok) break;
+      const int ntok = flags[st];
+      if (ntok < 0) poisoned = true;
+      const T* kbase = reinterpret_cast<const T*>(smem + st * 2 * L.part_bytes);
+      const T* vbase = reinterpret_cast<const T*>(smem + st * 2 * L.part_bytes + L.part_bytes);
+      // token of slot tg at step i: sub + WH * (tg + kTg * i)
+      for (int i0 = 0; sub + WH * (C::kTg * i0) < ntok; i0 += C::kBatch) {
+        float sc[C::kBatch][C::kGL];
+        const bool full = sub + WH * (C::kTg - 1 + C::kTg * (i0 + C::kBatch - 1)) < ntok;
+#pragma unroll
+        for (int b = 0; b < C::kBatch; ++b) {
+          const int t = sub + WH * (tg + C::kTg * (i0 + b));
+          float2 part[C::kGL];
+#pragma unroll
+          for (int h = 0; h < C::kGL; ++h) part[h] = make_float2(0.f, 0.f);
+          if (full || t < ntok) {
+            const T* krow = kbase + (t * HKV + g) * D;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+              float2 kf[C::kVec / 2];
+              load_pairs(krow + (kl + C::kLpt * c) * C::kVec, kf);
+#pragma unroll
+              for (int i = 0; i < C::kVec / 2; ++i)
+#pragma unroll
+                for (int h = 0; h < C::kGL; ++h)
+                  part[h] = __ffma2_rn(qf[h][c * (C::kVec / 2) + i], kf[i], part[h]);
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < C::kGL; ++h) sc[b][h] = part[h].x + part[h].y;
+        }
+        // complete the dot products across the lanes sharing a (token, head group)
+#pragma unroll
+        for (int off = C::kLpt / 2; off >= 1; off >>= 1)
+#pragma unroll
+          for (int b = 0; b < C::kBatch; ++b)
+#pragma unroll
+            for (int h = 0; h < C::kGL; ++h) sc[b][h] += __shfl_xor_sync(0xffffffffu, sc[b][h], off);
+        // online softmax (lazy max, warp-uniform rescale decision)
+        float mx[C::kGL];
+        bool need = false;
+#pragma unroll
+        for (int h = 0; h < C::kGL; ++h) {
+          mx[h] = -INFINITY;
+#pragma unroll
+          for (int b = 0; b < C::kBatch; ++b) {
+            const int t = sub + WH * (tg + C::kTg * (i0 + b));
+            if (full || t < ntok) mx[h] = fmaxf(mx[h], sc[b][h]);
+          }
+          need |= mx[h] > m[h] + kRescaleThreshold;
+        }
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int h = 0; h < C::kGL; ++h) {
+            const float mn = mx[h] > m[h] + kRescaleThreshold ? mx[h] : m[h];
+            const float a = merge_factor(m[h], mn);
+            l[h] *= a;
+#pragma unroll
+            for (int i = 0; i < C::kPairs; ++i)
+              acc[h][i] = make_float2(acc[h][i].x * a, acc[h][i].y * a);
+            m[h] = mn;
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < C::kBatch; ++b) {
+          const int t = sub + WH * (tg + C::kTg * (i0 + b));
+          const bool valid = full || t < ntok;
+#pragma unroll
+          for (int h = 0; h < C::kGL; ++h) {
+            const float w = valid ? fast_exp2(sc[b][h] - m[h]) : 0.f;
+            sc[b][h] = w;
+            l[h] += w;
+          }
+        }
+        // P.V
+#pragma unroll
+        for (int b = 0; b < C::kBatch; ++b) {
+          const int t = sub + WH * (tg + C::kTg * (i0 + b));
+          if (full || t < ntok) {
+            const T* vrow = vbase + (t * HKV + g) * D;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+              float2 vf[C::kVec / 2];
+              load_pairs(vrow + (kl + C::kLpt * c) * C::kVec, vf);
+#pragma unroll
+              for (int h = 0; h < C::kGL; ++h) {
+                const float2 w2 = make_float2(sc[b][h], sc[b][h]);
+#pragma unroll
+                for (int i = 0; i < C::kVec / 2; ++i)
+                  acc[h][c * (C::kVec / 2) + i] = __ffma2_rn(w2, vf[i], acc[h][c * (C::kVec / 2) + i]);
+              }
+            }
+          }
+        }
+      }
+      // stage consumed by this warp; the last warp to finish refills it
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        const int prev = atomicAdd(&done[st], 1);
+        if (prev == kWarps - 1) {
+          done[st] = 0;
+          __threadfence_block();
+          if (u + L.stages < n_units) issue(u + L.stages);
+        }
+      }
+    }
+    if (!ok) break;
+
+    // ------------------------------------------------------------ finish s
+    // 1. merge the token slots of the warp (lanes with equal head group and kl)
+#pragma unroll
+    for (int off = C::kLanesTok; off < 32; off <<= 1) {
+#pragma unroll
+      for (int h = 0; h < C::kGL; ++h) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
+        const float lo_ = __shfl_xor_sync(0xffffffffu, l[h], off);
+        const float mn = fmaxf(m[h], mo);
+        const float a = merge_factor(m[h], mn);
+        const float b = merge_factor(mo, mn);
+        l[h] = l[h] * a + lo_ * b;
+#pragma unroll
+        for (int i = 0; i < C::kPairs; ++i) {
+          const float ox = __shfl_xor_sync(0xffffffffu, acc[h][i].x, off);
+          const float oy = __shfl_xor_sync(0xffffffffu, acc[h][i].y, off);
+          acc[h][i] = make_float2(acc[h][i].x * a + ox * b, acc[h][i].y * a + oy * b);
+        }
+        m[h] = mn;
+      }
+    }
+    // 2. merge the warps that share a KV head through shared memory; the hand
+    //    over is ordered by two mbarriers per KV head (bounded waits)
+    if constexpr (WH > 1) {
+      const uint32_t ph = static_cast<uint32_t>(merges & 1);
+      float* slot_base = merge + g * (WH - 1) * G * (D + 2);
+      if (sub > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&merge_empty[g], ph ^ 1u));
+        if (ok && tg == 0) {
+          float* slot = slot_base + (sub - 1) * G * (D + 2);
+#pragma unroll
+          for (int h = 0; h < C::kGL; ++h) {
+            float* hs = slot + (hg * C::kGL + h) * (D + 2);
+            if (kl == 0) {
+              hs[D] = m[h];
+              hs[D + 1] = l[h];
+            }
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+#pragma unroll
+              for (int i = 0; i < C::kVec / 2; ++i) {
+                const int dim = (kl + C::kLpt * c) * C::kVec + 2 * i;
+                hs[dim] = acc[h][c * (C::kVec / 2) + i].x;
+                hs[dim + 1] = acc[h][c * (C::kVec / 2) + i].y;
+              }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&merge_full[g]);
+      } else {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&merge_full[g], ph));
+        if (ok) {
+          for (int w2 = 1; w2 < WH; ++w2) {
+            const float* slot = slot_base + (w2 - 1) * G * (D + 2);
+#pragma unroll
+            for (int h = 0; h < C::kGL; ++h) {
+              const float* hs = slot + (hg * C::kGL + h) * (D + 2);
+              const float mo = hs[D], lo_ = hs[D + 1];
+              const float mn = fmaxf(m[h], mo);
+              const float a = merge_factor(m[h], mn);
+              const float b = merge_factor(mo, mn);
+              l[h] = l[h] * a + lo_ * b;
+#pragma unroll
+              for (int c = 0; c < C::kChunks; ++c)
+#pragma unroll
+                for (int i = 0; i < C::kVec / 2; ++i) {
+                  const int dim = (kl + C::kLpt * c) * C::kVec + 2 * i;
+                  float2& r = acc[h][c * (C::kVec / 2) + i];
+                  r = make_float2(r.x * a + hs[dim] * b, r.y * a + hs[dim + 1] * b);
+                }
+              m[h] = mn;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&merge_empty[g]);
+      }
+      ++merges;
+      if (!ok) break;
+    }
+    // 3. write: the final row when this CTA saw the whole sequence, else a partial
+    if (sub == 0 && tg == 0) {
+      if (whole) {
+        T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(row) * p.hq + head0) * D;
+#pragma unroll
+        for (int h = 0; h < C::kGL; ++h) {
+          const float inv = poisoned ? 0.f : 1.f / l[h];
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c) {
+            const int dim0 = (kl + C::kLpt * c) * C::kVec;
+            if constexpr (sizeof(T) == 2) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 r = acc[h][c * 4 + i];
+                const __nv_bfloat162 bb = __floats2bfloat162_rn(r.x * inv, r.y * inv);
+                w[i] = *reinterpret_cast<const uint32_t*>(&bb);
+              }
+              *reinterpret_cast<uint4*>(orow + h * D + dim0) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+              const float2 r0 = acc[h][c * 2], r1 = acc[h][c * 2 + 1];
+              *reinterpret_cast<float4*>(orow + h * D + dim0) =
+                  make_float4(r0.x * inv, r0.y * inv, r1.x * inv, r1.y * inv);
+            }
+          }
+        }
+      } else {
+        const int64_t slot = static_cast<int64_t>(blockIdx.x) + s;
+#pragma unroll
+        for (int h = 0; h < C::kGL; ++h) {
+          const int hh = head0 + h;
+          if (kl == 0) p.ws_ml[slot * p.hq + hh] = make_float2(m[h], poisoned ? -1.f : l[h]);
+          float* arow = p.ws_acc + (slot * p.hq + hh) * D;
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c) {
+            const int dim0 = (kl + C::kLpt * c) * C::kVec;
+#pragma unroll
+            for (int i = 0; i < C::kVec / 4; ++i) {
+              const float2 r0 = acc[h][c * (C::kVec / 2) + 2 * i];
+              const float2 r1 = acc[h][c * (C::kVec / 2) + 2 * i + 1];
+              *reinterpret_cast<float4*>(arow + dim0 + 4 * i) = make_float4(r0.x, r0.y, r1.x, r1.y);
+            }
+          }
+        }
+      }
+    }
+  }
+  if (!ok && lane == 0) status_or(p.d_status, PA_STATUS_TIMEOUT);
+  pdl_launch_dependents();
+}
+
+// Merge the partials of sequences that straddle CTAs: o = sum_c a_c acc_c /
+// sum_c a_c l_c with a_c = 2^(m_c - max_c m_c). One warp per (sequence,
+// head); partials are read four at a time so their loads overlap.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p, int grid) {
+  pdl_wait_primary();
+  constexpr int kPer = D / 32;  // elements per lane
+  const int s = blockIdx.x;
+  const int* prefix = p.ws_prefix;
+  const int64_t B = prefix[p.num_seqs];
+  const int64_t a0 = prefix[s], a1 = prefix[s + 1];
+  if (a1 <= a0) return;
+  // CTA c covers blocks [c*B/grid, (c+1)*B/grid)
+  const int64_t c_first = ((a0 + 1) * grid - 1) / B;
+  const int64_t c_last = (a1 * grid - 1) / B;
+  if (c_first == c_last) return;  // finished by the decode kernel
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = query_row(p, s);
+  T* orow = static_cast<T*>(p.out) + static_cast<int64_t>(row) * p.hq * D;
+  for (int h = warp; h < p.hq; h += blockDim.x >> 5) {
+    float m = -INFINITY, l = 0.f;
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    bool poisoned = false;
+    for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+      float2 ml[4];
+      float v[4][kPer];
+      bool use[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t c = c0 + j;
+        use[j] = c <= c_last && (c * B / grid != (c + 1) * B / grid);
+        if (use[j]) {
+          ml[j] = p.ws_ml[(c + s) * p.hq + h];
+          const float* src = p.ws_acc + ((c + s) * p.hq + h) * D + lane * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; e += 2) {
+            const float2 x = *reinterpret_cast<const float2*>(src + e);
+            v[j][e] = x.x;
+            v[j][e + 1] = x.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (!use[j]) continue;
+        poisoned |= ml[j].y < 0.f;
+        const float mn = fmaxf(m, ml[j].x);
+        const float a = merge_factor(m, mn), b = merge_factor(ml[j].x, mn);
+        l = l * a + ml[j].y * b;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) acc[e] = acc[e] * a + v[j][e] * b;
+        m = mn;
+      }
+    }
+    const float inv = poisoned ? 0.f : 1.f / l;
+    T* dst = orow + h * D + lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) dst[e] = from_float<T>(acc[e] * inv);
+  }
+}
+
+template <typename T, int D, int G, int WH>
+cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int hkv = kWarps / WH;
+  const int elt = sizeof(T);
+  const int token_bytes = hkv * D * elt;
+  // tokens of one block moved per stage: whole blocks when a K+V block fits 64 KB
+  int tpu = kBlockSize;
+  while (tpu > 4 && 2 * tpu * token_bytes > 64 * 1024) tpu /= 2;
+  const int smem_limit = 227 * 1024 - 1024;  // leave room for static shared memory
+  SmemLayout L = make_layout(4, tpu, hkv, D, elt, WH, G, a.num_seqs);
+  if (L.total > smem_limit) L = make_layout(3, tpu, hkv, D, elt, WH, G, a.num_seqs);
+  if (L.total > smem_limit) L = make_layout(2, tpu, hkv, D, elt, WH, G, a.num_seqs);
+  if (L.total > smem_limit) return cudaErrorInvalidValue;
+
+  int grid = a.grid_override > 0 ? a.grid_override : device_sm_count();
+  grid = std::min(grid, kMaxDecodeCtas);
+
+  DecodeParams p;
+  p.k_pool = static_cast<const char*>(a.pool.k);
+  p.v_pool = static_cast<const char*>(a.pool.v);
+  p.num_blocks = a.pool.num_blocks;
+  p.hkv = hkv;
+  p.hq = a.num_q_heads;
+  p.q = a.q;
+  p.out = a.out;
+  p.cu_q_lens = a.cu_q_lens;
+  p.num_seqs = a.num_seqs;
+  p.num_rows = a.num_rows;
+  p.block_tables = a.block_tables;
+  p.max_blocks = a.max_blocks_per_seq;
+  p.context_lens = a.context_lens;
+  p.scale_log2 = a.scale * kLog2e;
+  char* ws = static_cast<char*>(a.workspace);
+  const size_t prefix_bytes = align_up_sz((a.num_seqs + 1) * 4, 256);
+  const size_t slots = static_cast<size_t>(kMaxDecodeCtas) + a.num_seqs;
+  p.ws_prefix = reinterpret_cast<int*>(ws);
+  p.ws_ml = reinterpret_cast<float2*>(ws + prefix_bytes);
+  p.ws_acc = reinterpret_cast<float*>(ws + prefix_bytes + align_up_sz(slots * a.num_q_heads * 8, 256));
+  p.d_status = a.d_status;
+  p.L = L;
+
+  auto kern = decode_kernel<T, D, G, WH>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kThreads, L.total, stream>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  // merge kernel, launched with programmatic stream serialization so its
+  // launch overlaps the decode kernel's tail (it waits with griddepcontrol.wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_seqs);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<T, D>, p, grid);
+}
+
+template <typename T, int D, int G>
+cudaError_t dispatch_wh(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.pool.num_kv_heads) {
+    case 8: return launch_typed<T, D, G, 1>(a, stream);
+    case 4: return launch_typed<T, D, G, 2>(a, stream);
+    case 2: return launch_typed<T, D, G, 4>(a, stream);
+    case 1: return launch_typed<T, D, G, 8>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+// Dispatch on the GQA group and the number of KV heads for one (dtype, head_dim).
+template <typename T, int D>
+cudaError_t dispatch_decode_d(const DecodeArgs& a, int group, cudaStream_t stream) {
+  switch (group) {
+    case 1: return dispatch_wh<T, D, 1>(a, stream);
+    case 2: return dispatch_wh<T, D, 2>(a, stream);
+    case 4: return dispatch_wh<T, D, 4>(a, stream);
+    case 8: return dispatch_wh<T, D, 8>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pa

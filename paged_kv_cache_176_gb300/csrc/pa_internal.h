@@ -10,6 +10,10 @@
 
 namespace pa {
 
+constexpr int kMaxDecodeCtas = 1024;  // decode workspace holds this many CTA partial slots
+
+inline size_t align_up_sz(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
 struct PoolView {
   void* k;
   void* v;
@@ -50,6 +54,13 @@ struct DecodeArgs {
   int grid_override;         // > 0: number of persistent CTAs (tuning / tests)
 };
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim);
+// per (dtype, head_dim) entry points, one translation unit each
+cudaError_t decode_f32_d64(const DecodeArgs& a, int group, cudaStream_t stream);
+cudaError_t decode_f32_d128(const DecodeArgs& a, int group, cudaStream_t stream);
+cudaError_t decode_f32_d256(const DecodeArgs& a, int group, cudaStream_t stream);
+cudaError_t decode_bf16_d64(const DecodeArgs& a, int group, cudaStream_t stream);
+cudaError_t decode_bf16_d128(const DecodeArgs& a, int group, cudaStream_t stream);
+cudaError_t decode_bf16_d256(const DecodeArgs& a, int group, cudaStream_t stream);
 bool decode_supported(int dtype, int head_dim, int group, int num_kv_heads);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
