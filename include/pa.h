@@ -132,6 +132,33 @@ PA_API int pa_decode(const pa_kv_pool* pool, void* out, const void* q, int num_s
               size_t workspace_bytes, int* d_status, void* stream);
 
 /*
+ * pa_decode without a workspace argument, for callers that cannot allocate
+ * device memory around the call (for example a host framework that plans all
+ * device buffers itself and does not let libraries call cudaMalloc, or a
+ * latency-critical loop where an allocation, which can synchronize the device
+ * or fail under memory pressure, is not allowed). The pages describe no such
+ * entry point; it has no counterpart there.
+ *
+ * Same arguments, kernels and results as pa_decode, minus workspace and
+ * workspace_bytes. The split-K scratch is a static device array of
+ * PA_DECODE_STATIC_WS_BYTES inside libpa, held on every GPU that loads the
+ * library until the process exits; the call allocates nothing.
+ *  - Sizes whose pa_decode_workspace_size() exceeds PA_DECODE_STATIC_WS_BYTES
+ *    are rejected with PA_EWORKSPACE before anything is enqueued.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make the
+ *    first call on a device before any stream capture.
+ *  - Every call uses the same array, which keeps the previous call's
+ *    contents; nothing in it needs to start at zero. Calls that overlap on the
+ *    GPU (other streams, other host threads) race on it: serialize them.
+ */
+#define PA_DECODE_STATIC_WS_BYTES (((size_t)32) << 20)
+PA_API int pa_decode_static_ws(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+                               int num_q_heads, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* context_lens, float scale,
+                               int* d_status, void* stream);
+
+/*
  * Tuning knob: the number of persistent CTAs the decode kernel runs (0, the
  * default, means one per SM of the current device; values above 1024 are
  * clamped). It applies to later pa_decode / pa_mixed_step calls from any

@@ -82,6 +82,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_mixed_step.argtypes = [PP, P, P, P, I, I, I, P, P, I, F, I, P, P, P, P, SZ, P, P]
         lib.pa_set_decode_ctas.restype = I
         lib.pa_set_decode_ctas.argtypes = [I]
+        lib.pa_decode_static_ws.restype = I
+        lib.pa_decode_static_ws.argtypes = [PP, P, P, I, I, P, I, P, F, P, P]
         _lib = lib
         return lib
 
@@ -189,6 +191,27 @@ def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale: float, 
            lib.pa_decode(ctypes.byref(pool), _ptr(out), _ptr(q), S, hq, _ptr(block_tables), mb,
                          _ptr(context_lens), float(scale), _ptr(ws), ws.numel() * ws.element_size(),
                          _ptr(d_status), _stream(stream)))
+    return out
+
+
+PA_DECODE_STATIC_WS_BYTES = 32 << 20
+
+
+def pa_decode_static_ws(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,
+                        d_status=None, stream=None):
+    """Decode attention that allocates nothing: the split-K scratch is a
+    static device array inside libpa (see include/pa.h). For callers that
+    cannot allocate device memory around the call. Returns out."""
+    lib = load()
+    pool = make_pool(k_pool, v_pool)
+    S, hq, d = q.shape
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    mb = int(block_tables.shape[1])
+    _check("pa_decode_static_ws",
+           lib.pa_decode_static_ws(ctypes.byref(pool), _ptr(out), _ptr(q), S, hq,
+                                   _ptr(block_tables), mb, _ptr(context_lens), float(scale),
+                                   _ptr(d_status), _stream(stream)))
     return out
 
 
