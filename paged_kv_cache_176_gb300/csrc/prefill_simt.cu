@@ -237,14 +237,4 @@ cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream) {
   return launch_simt_typed<float>(a, stream);
 }
 
-bool prefill_supported(int dtype, int head_dim, int group) {
-  if (dtype != PA_F32 && dtype != PA_BF16) return false;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return false;
-  return group == 1 || group == 2 || group == 4 || group == 8;
-}
-
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  return launch_prefill_simt(a, stream);
-}
-
 }  // namespace pa

@@ -1,0 +1,498 @@
+// prefill_tc.cu -- chunked-prefill attention on the tcgen05 tensor cores (bf16).
+//
+// A prefill chunk of q_len tokens of sequence s (context ctx, which includes
+// the chunk) attends causally over absolute positions: query row i sits at
+// position ctx - q_len + i and sees keys 0 .. that position, i.e. the cached
+// keys of all earlier chunks plus its own tokens up to itself ("Chunked
+// Prefill" glossary page, how chunked prefill works: the mask
+// ones(end - start, end).tril(diagonal = start)). Keys and values are gathered
+// through the sequence's block table (K_r = gather(K_pool, table_r), the
+// gather figure of the "C13 L2 serving" page).
+//
+// GB300 design (one CTA per 128 query rows of one KV head):
+//  * The 128 rows are 128/G tokens x the G query heads that share the KV head,
+//    so one K/V tile in shared memory serves the whole GQA group.
+//  * Warp 0 moves data with TMA: the Q tile once, then K/V tiles of 128 keys
+//    (8 pool blocks) into a two-stage ring; each block is one 3-D tiled copy
+//    (64 head-dim columns x 16 tokens, 128-byte swizzle) straight out of the
+//    paged pool, so the gather costs no extra pass.
+//  * Warp 1 owns 512 TMEM columns and issues the MMAs from one thread:
+//    S = Q K^T (128 x 128, fp32, double-buffered in TMEM) and O += P V
+//    (128 x head_dim, fp32 in TMEM), with tcgen05.commit signalling mbarriers.
+//  * Warps 2-5 hold one query row per thread: they read S from TMEM, apply the
+//    causal mask and the online softmax in the log2 domain, write P as bf16
+//    into shared memory for the P.V MMA, and rescale O in TMEM only when the
+//    row max grows by more than 8 (lazy rescaling). Masked keys get weight 0.
+//  * Value rows past the context in the last key tile are zeroed before the
+//    P.V MMA, so stale or NaN pool slots never reach the result.
+//  * Every wait is bounded; a timeout sets PA_STATUS_TIMEOUT and the CTA
+//    leaves after releasing its TMEM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+#include "tc_common.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kD = 128;              // head_dim of the tensor-core path
+constexpr int kRowsTile = 128;       // query rows per CTA (MMA M)
+constexpr int kKeysTile = 128;       // keys per tile (MMA N of Q K^T)
+constexpr int kBlocksTile = kKeysTile / kBlockSize;
+constexpr int kThreadsTc = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kHalf = 16384;         // one 64-column half of a 128-row bf16 tile
+
+// shared memory layout (offsets from a 1024-byte aligned base)
+constexpr int kOffQ = 0;                          // 2 halves
+constexpr int kOffKV = 2 * kHalf;                 // 2 stages x (K: 2 halves, V: 2 halves)
+constexpr int kStageBytes = 4 * kHalf;
+constexpr int kOffP = kOffKV + 2 * kStageBytes;   // 2 halves (keys 0-63, 64-127)
+constexpr int kOffBar = kOffP + 2 * kHalf;
+constexpr int kSmemTc = kOffBar + 256 + 1024;     // + barriers + alignment slack
+
+// TMEM columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0;     // S buffers at 0 and 128
+constexpr uint32_t kColO = 256;    // O accumulator
+
+struct TcParams {
+  const int32_t* cu_q_lens;
+  const int32_t* context_lens;
+  const int32_t* block_tables;
+  void* out;
+  int num_seqs, num_rows, hq, hkv, group, max_blocks;
+  int64_t num_blocks;
+  float scale_log2;
+  int* d_status;
+};
+
+struct TcBarriers {
+  uint64_t q_full;
+  uint64_t kv_full[2];
+  uint64_t kv_empty[2];
+  uint64_t s_full[2];
+  uint64_t s_empty[2];
+  uint64_t p_full;
+  uint64_t pv_done;
+  uint32_t tmem_base;
+  int bad_block;
+  int abort;
+};
+
+__device__ __forceinline__ int tc_tiles(const TcParams& p, int s, int tq) {
+  const int q0 = p.cu_q_lens[s], q1 = p.cu_q_lens[s + 1];
+  if (q0 < 0 || q1 > p.num_rows || q1 - q0 <= 1) return 0;
+  return (q1 - q0 + tq - 1) / tq;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace
+}  // namespace pa
+
+namespace pa {
+namespace {
+
+constexpr int kOffPrefix = kOffBar + 256;  // tile prefix over sequences
+
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+  extern __shared__ char smem_raw[];
+  char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  TcBarriers& bar = *reinterpret_cast<TcBarriers*>(smem + kOffBar);
+  int* prefix = reinterpret_cast<int*>(smem + kOffPrefix);
+  __shared__ int warp_sums[kThreadsTc / 32];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.group;
+  const int tq = kRowsTile / G;  // tokens per tile
+  const int g = blockIdx.y;      // KV head
+
+  // this CTA's (sequence, tile); tiles run from the last (longest) one down
+  block_exclusive_scan<kThreadsTc>(
+      p.num_seqs, [&](int i) { return tc_tiles(p, i, tq); }, prefix, warp_sums);
+  const int total = prefix[p.num_seqs];
+  if (static_cast<int>(blockIdx.x) >= total) return;
+  const int t_global = total - 1 - static_cast<int>(blockIdx.x);
+  const int s = upper_index(prefix, p.num_seqs, t_global);
+  const int tile = t_global - prefix[s];
+  const int q0 = p.cu_q_lens[s];
+  const int q_len = p.cu_q_lens[s + 1] - q0;
+  const int ctx = p.context_lens[s];
+  const int tok0 = tile * tq;
+  const int ntok = min(tq, q_len - tok0);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  if (q_len > ctx || ctx > p.max_blocks * kBlockSize) {
+    if (tid == 0) status_or(p.d_status, PA_STATUS_BAD_LENGTH);
+    for (int i = tid; i < ntok * G * kD; i += kThreadsTc) {
+      const int tok = i / (G * kD), rem = i % (G * kD);
+      out[(static_cast<int64_t>(q0 + tok0 + tok) * p.hq + g * G) * kD + rem] = __float2bfloat16_rn(0.f);
+    }
+    return;
+  }
+  const int max_pos = ctx - q_len + tok0 + ntok - 1;  // last row's absolute position
+  const int n_kt = max_pos / kKeysTile + 1;           // key tiles
+  const int nblk = max_pos / kBlockSize + 1;          // pool blocks holding keys 0..max_pos
+
+  if (tid == 0) {
+    mbar_init(&bar.q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.kv_full[i], 1);
+      mbar_init(&bar.kv_empty[i], 1);
+      mbar_init(&bar.s_full[i], 1);
+      mbar_init(&bar.s_empty[i], 4);
+    }
+    mbar_init(&bar.p_full, 4);
+    mbar_init(&bar.pv_done, 1);
+    bar.bad_block = 0;
+    bar.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bar.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bar.tmem_base;
+  float row_sum = 0.f;  // softmax threads: sum of the row's weights
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_q);
+      tc::prefetch_tmap(&tm_k);
+      tc::prefetch_tmap(&tm_v);
+      mbar_arrive_expect_tx(&bar.q_full, 2 * kHalf);
+      tc::tma_load_3d(smem + kOffQ, &tm_q, 0, g * G, q0 + tok0, &bar.q_full);
+      tc::tma_load_3d(smem + kOffQ + kHalf, &tm_q, 64, g * G, q0 + tok0, &bar.q_full);
+      for (int j = 0; j < n_kt; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait_bounded(&bar.kv_empty[st], ((j >> 1) & 1) ^ 1)) {
+          atomicOr(&bar.abort, 1);
+          break;
+        }
+        const int b0 = j * kBlocksTile;
+        const int nb = min(kBlocksTile, nblk - b0);
+        char* sk = smem + kOffKV + st * kStageBytes;
+        char* sv = sk + 2 * kHalf;
+        mbar_arrive_expect_tx(&bar.kv_full[st], nb * 4 * (kBlockSize * 128));
+        for (int b = 0; b < nb; ++b) {
+          int phys = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + b0 + b];
+          if (phys < 0 || phys >= p.num_blocks) {  // keep the copy in bounds, zero the output
+            bar.bad_block = 1;
+            status_or(p.d_status, PA_STATUS_BAD_BLOCK);
+            phys = 0;
+          }
+          const int row = phys * kBlockSize;
+          const int off = b * kBlockSize * 128;
+          tc::tma_load_3d(sk + off, &tm_k, 0, g, row, &bar.kv_full[st]);
+          tc::tma_load_3d(sk + kHalf + off, &tm_k, 64, g, row, &bar.kv_full[st]);
+          tc::tma_load_3d(sv + off, &tm_v, 0, g, row, &bar.kv_full[st]);
+          tc::tma_load_3d(sv + kHalf + off, &tm_v, 64, g, row, &bar.kv_full[st]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = tc::idesc_bf16_f32(kRowsTile, kKeysTile, false, false);
+      const uint32_t id_pv = tc::idesc_bf16_f32(kRowsTile, kD, false, true);
+      const uint32_t sQ = smem_addr(smem + kOffQ);
+      const uint32_t sP = smem_addr(smem + kOffP);
+      // S(j) = Q K_j^T into TMEM buffer j % 2
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait_bounded(&bar.kv_full[st], (j >> 1) & 1)) return false;
+        if (!mbar_wait_bounded(&bar.s_empty[st], ((j >> 1) & 1) ^ 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t sK = smem_addr(smem + kOffKV + st * kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem + kColS0 + st * kKeysTile, tc::smem_desc(sQ + o, 16, 1024),
+                       tc::smem_desc(sK + o, 16, 1024), id_qk, kk > 0);
+        }
+        tc::mma_commit(&bar.s_full[st]);
+        return true;
+      };
+      bool ok = mbar_wait_bounded(&bar.q_full, 0);
+      if (ok) ok = issue_s(0);
+      if (ok && n_kt > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < n_kt; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait_bounded(&bar.p_full, j & 1)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        // O += P_j V_j (V is MN-major: head_dim contiguous)
+        const uint32_t sV = smem_addr(smem + kOffKV + st * kStageBytes + 2 * kHalf);
+#pragma unroll
+        for (int kk = 0; kk < kKeysTile / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem + kColO, tc::smem_desc(sP + o, 16, 1024),
+                       tc::smem_desc(sV + kk * (16 * 128), kHalf, 1024), id_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&bar.kv_empty[st]);
+        tc::mma_commit(&bar.pv_done);
+        if (j + 2 < n_kt) ok = issue_s(j + 2);
+      }
+      if (!ok) atomicOr(&bar.abort, 1);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quad = warp & 3;                 // TMEM lane quarter this warp may access
+    const int r = quad * 32 + lane;            // tile row owned by this thread
+    const int ri = r / G, rh = r % G;          // token within the tile, head within the group
+    const int pos = ri < ntok ? ctx - q_len + tok0 + ri : -1;  // absolute position (-1: padding row)
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    char* sP = smem + kOffP;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      const int buf = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.s_full[buf], (j >> 1) & 1));
+      if (!ok) break;
+      tc::fence_after_sync();
+      float sc[kKeysTile];
+      {
+        uint32_t raw[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(trow + kColS0 + buf * kKeysTile + c * 32, raw[c]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sc[c * 32 + e] = __uint_as_float(raw[c][e]);
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.s_empty[buf]);
+      // causal mask over absolute positions, scores in the log2 domain
+      const int key0 = j * kKeysTile;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKeysTile; ++c) {
+        const float v = (key0 + c <= pos) ? sc[c] * p.scale_log2 : -INFINITY;
+        sc[c] = v;
+        mx = fmaxf(mx, v);
+      }
+      // P_{j-1} V_{j-1} must be complete before O is rescaled or P rewritten
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.pv_done, (j - 1) & 1));
+        if (!ok) break;
+        tc::fence_after_sync();
+      }
+      const bool need = mx > m + 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float mn = need ? mx : m;
+        const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
+        l *= alpha;
+        m = mn;
+        if (j > 0) {  // O holds tiles 0 .. j-1: rescale this warp's rows in TMEM
+#pragma unroll
+          for (int c = 0; c < kD / 32; ++c) {
+            uint32_t o[32];
+            tc::tmem_ld32(trow + kColO + c * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tc::tmem_st32(trow + kColO + c * 32, o);
+          }
+          tc::tmem_wait_st();
+        }
+      }
+      // P = 2^(s - m) as bf16 into the 128-byte swizzled P tile (row r)
+      float rs = 0.f;
+#pragma unroll
+      for (int kc = 0; kc < kKeysTile / 8; ++kc) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = sc[kc * 8 + 2 * e], b = sc[kc * 8 + 2 * e + 1];
+          const float pa = a == -INFINITY ? 0.f : ex2(a - m);
+          const float pb = b == -INFINITY ? 0.f : ex2(b - m);
+          rs += pa + pb;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
+          w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        *reinterpret_cast<uint4*>(sP + (kc >> 3) * kHalf + tc::sw128_offset(r, kc & 7)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l += rs;
+      // last tile: zero the value rows no key of this CTA may use
+      if (j == n_kt - 1) {
+        const int st = j & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.kv_full[st], (j >> 1) & 1));
+        if (!ok) break;
+        // rows past the context hold stale or poisoned slots; rows past the
+        // last loaded block were never written by this CTA
+        if (key0 + r >= min(ctx, nblk * kBlockSize)) {
+          char* sv = smem + kOffKV + st * kStageBytes + 2 * kHalf;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(sv + h * kHalf + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();  // P (and zeroed V rows) visible to the tensor cores
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.p_full);
+    }
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.pv_done, (n_kt - 1) & 1));
+      if (ok) tc::fence_after_sync();
+    }
+    if (!ok) atomicOr(&bar.abort, 1);
+    row_sum = l;
+  }
+
+  __syncthreads();  // every role done issuing; the last P.V is complete
+  if (warp >= 2) {
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int ri = r / G, rh = r % G;
+    if (bar.abort == 0) {
+      // epilogue: O / l as bf16 (every lane loads: tcgen05.ld is warp-collective)
+      const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      uint32_t raw[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(trow + kColO + c * 32, raw[c]);
+      tc::tmem_wait_ld();
+      if (ri < ntok) {
+        const float inv = bar.bad_block ? 0.f : 1.f / row_sum;
+        __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + tok0 + ri) * p.hq + g * G + rh) * kD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(raw[c][e + 2 * k]) * inv,
+                                                              __uint_as_float(raw[c][e + 2 * k + 1]) * inv);
+              w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(orow + c * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+      }
+    } else if (r == 0) {
+      status_or(p.d_status, PA_STATUS_TIMEOUT);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+}  // namespace pa
+
+namespace pa {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no libcuda link).
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor {inner, mid, outer} with 128-byte swizzled boxes.
+bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
+               uint32_t box_inner, uint32_t box_mid, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {inner, mid, outer};
+  const cuuint64_t strides[2] = {inner * 2, inner * mid * 2};  // bytes, dims 1 and 2
+  const cuuint32_t box[3] = {box_inner, box_mid, box_outer};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_supported(const PrefillArgs& a) {
+  const int group = a.num_q_heads / a.pool.num_kv_heads;
+  return a.pool.dtype == PA_BF16 && a.pool.head_dim == kD && kRowsTile % group == 0 &&
+         group <= 8 && encode_tiled() != nullptr;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
+  const int hkv = a.pool.num_kv_heads;
+  const int group = a.num_q_heads / hkv;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap(&tq, a.q, kD, a.num_q_heads, a.num_tokens, 64, group, kRowsTile / group) ||
+      !make_tmap(&tk, a.pool.k, kD, hkv, a.pool.num_blocks * kBlockSize, 64, 1, kBlockSize) ||
+      !make_tmap(&tv, a.pool.v, kD, hkv, a.pool.num_blocks * kBlockSize, 64, 1, kBlockSize))
+    return cudaErrorInvalidValue;
+  TcParams p;
+  p.cu_q_lens = a.cu_q_lens;
+  p.context_lens = a.context_lens;
+  p.block_tables = a.block_tables;
+  p.out = a.out;
+  p.num_seqs = a.num_seqs;
+  p.num_rows = a.num_tokens;
+  p.hq = a.num_q_heads;
+  p.hkv = hkv;
+  p.group = group;
+  p.max_blocks = a.max_blocks_per_seq;
+  p.num_blocks = a.pool.num_blocks;
+  p.scale_log2 = a.scale * kLog2e;
+  p.d_status = a.d_status;
+  const int tq_tokens = kRowsTile / group;
+  const int tiles = (a.num_tokens + tq_tokens - 1) / tq_tokens + a.num_seqs;  // upper bound
+  const int smem = kOffPrefix + (a.num_seqs + 1) * 4 + 1024;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  cudaError_t err =
+      cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  prefill_tc_kernel<<<dim3(tiles, hkv), kThreadsTc, smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_supported(int dtype, int head_dim, int group) {
+  if (dtype != PA_F32 && dtype != PA_BF16) return false;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return false;
+  return group == 1 || group == 2 || group == 4 || group == 8;
+}
+
+// bf16 with head_dim 128 runs on the tensor cores; the other shapes and fp32
+// run on the CUDA-core kernel (prefill_simt.cu).
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  if (a.num_tokens == 0 || a.num_seqs == 0) return cudaSuccess;
+  if (tc_supported(a)) return launch_prefill_tc(a, stream);
+  return launch_prefill_simt(a, stream);
+}
+
+}  // namespace pa
