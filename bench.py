@@ -461,6 +461,8 @@ def main() -> None:
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--mixed-steps", type=int, default=200)
     ap.add_argument("--skip-mixed", action="store_true")
+    ap.add_argument("--only-mixed", action="store_true",
+                    help="run only the mixed step (profiling); prints its measurement")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=8.0)
@@ -477,7 +479,12 @@ def main() -> None:
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group(backend)
-    if args.impl == "reference":
+    if args.only_mixed and args.impl != "reference":
+        import torch
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+        torch.cuda.set_device(dev)
+        res = run_mixed(args, dev, torch.cuda.Stream(dev))
+    elif args.impl == "reference":
         res = run_reference(args, rank, world)
     else:
         res = run_gpu(args, rank, world)

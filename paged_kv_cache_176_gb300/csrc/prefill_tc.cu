@@ -43,16 +43,20 @@ constexpr int kD = 128;              // head_dim of the tensor-core path
 constexpr int kRowsTile = 128;       // query rows per CTA (MMA M)
 constexpr int kKeysTile = 128;       // keys per tile (MMA N of Q K^T)
 constexpr int kBlocksTile = kKeysTile / kBlockSize;
-constexpr int kThreadsTc = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kThreadsTc = 224;      // warp 0 K loads, warp 1 MMA, warps 2-5 softmax, warp 6 V loads
 constexpr int kHalf = 16384;         // one 64-column half of a 128-row bf16 tile
+constexpr int kTileBytes = 2 * kHalf;
+constexpr int kKStages = 3;          // K is released as soon as S = Q K^T is done
+constexpr int kVStages = 2;          // V is released after O += P V
 
 // shared memory layout (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;                          // 2 halves
-constexpr int kOffKV = 2 * kHalf;                 // 2 stages x (K: 2 halves, V: 2 halves)
-constexpr int kStageBytes = 4 * kHalf;
-constexpr int kOffP = kOffKV + 2 * kStageBytes;   // 2 halves (keys 0-63, 64-127)
-constexpr int kOffBar = kOffP + 2 * kHalf;
-constexpr int kSmemTc = kOffBar + 256 + 1024;     // + barriers + alignment slack
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffP = kOffV + kVStages * kTileBytes;  // also holds the tile prefix at start-up
+constexpr int kOffBar = kOffP + kTileBytes;
+constexpr int kSmemTc = kOffBar + 256 + 1024;         // + barriers + alignment slack
+constexpr int kMaxPrefixSeqs = kTileBytes / 4 - 1;
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
@@ -72,8 +76,10 @@ struct TcParams {
 
 struct TcBarriers {
   uint64_t q_full;
-  uint64_t kv_full[2];
-  uint64_t kv_empty[2];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t s_full[2];
   uint64_t s_empty[2];
   uint64_t p_full;
@@ -82,6 +88,7 @@ struct TcBarriers {
   int bad_block;
   int abort;
 };
+static_assert(sizeof(TcBarriers) <= 256, "barrier block");
 
 __device__ __forceinline__ int tc_tiles(const TcParams& p, int s, int tq) {
   const int q0 = p.cu_q_lens[s], q1 = p.cu_q_lens[s + 1];
@@ -101,8 +108,6 @@ __device__ __forceinline__ float ex2(float x) {
 namespace pa {
 namespace {
 
-constexpr int kOffPrefix = kOffBar + 256;  // tile prefix over sequences
-
 __global__ void __launch_bounds__(kThreadsTc, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -110,7 +115,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   extern __shared__ char smem_raw[];
   char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   TcBarriers& bar = *reinterpret_cast<TcBarriers*>(smem + kOffBar);
-  int* prefix = reinterpret_cast<int*>(smem + kOffPrefix);
   __shared__ int warp_sums[kThreadsTc / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -118,7 +122,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int tq = kRowsTile / G;  // tokens per tile
   const int g = blockIdx.y;      // KV head
 
-  // this CTA's (sequence, tile); tiles run from the last (longest) one down
+  // this CTA's (sequence, tile); tiles run from the last (longest) one down.
+  // The prefix lives in the P buffer, which is free until the softmax starts.
+  int* prefix = reinterpret_cast<int*>(smem + kOffP);
   block_exclusive_scan<kThreadsTc>(
       p.num_seqs, [&](int i) { return tc_tiles(p, i, tq); }, prefix, warp_sums);
   const int total = prefix[p.num_seqs];
@@ -146,9 +152,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   if (tid == 0) {
     mbar_init(&bar.q_full, 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&bar.k_full[i], 1);
+      mbar_init(&bar.k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&bar.v_full[i], 1);
+      mbar_init(&bar.v_empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar.kv_full[i], 1);
-      mbar_init(&bar.kv_empty[i], 1);
       mbar_init(&bar.s_full[i], 1);
       mbar_init(&bar.s_empty[i], 4);
     }
@@ -168,41 +180,61 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint32_t tmem = bar.tmem_base;
   float row_sum = 0.f;  // softmax threads: sum of the row's weights
 
+  // Block-table entries of key tile j, read as one batch of independent loads.
+  auto tile_blocks = [&](int j, int (&ph)[kBlocksTile]) -> int {
+    const int b0 = j * kBlocksTile;
+    const int nb = min(kBlocksTile, nblk - b0);
+    const int32_t* row = p.block_tables + static_cast<int64_t>(s) * p.max_blocks + b0;
+#pragma unroll
+    for (int b = 0; b < kBlocksTile; ++b) ph[b] = b < nb ? __ldg(row + b) : 0;
+    return nb;
+  };
+  // One producer per operand: TMA of K tiles (warp 0) or V tiles (warp 6),
+  // each 128 keys = 8 pool blocks x two 64-column halves.
+  auto produce = [&](const CUtensorMap* tm, int off, int stages, uint64_t* full, uint64_t* empty) {
+    int ph[kBlocksTile], phn[kBlocksTile];
+    int nb = tile_blocks(0, ph);
+    for (int j = 0; j < n_kt; ++j) {
+      const int st = j % stages;
+      const int nbn = j + 1 < n_kt ? tile_blocks(j + 1, phn) : 0;  // prefetch the next tile's table
+      if (!mbar_wait_bounded(&empty[st], ((j / stages) & 1) ^ 1)) {
+        atomicOr(&bar.abort, 1);
+        return;
+      }
+      char* dst = smem + off + st * kTileBytes;
+      mbar_arrive_expect_tx(&full[st], nb * 2 * (kBlockSize * 128));
+      for (int b = 0; b < nb; ++b) {
+        int phys = ph[b];
+        if (phys < 0 || phys >= p.num_blocks) {  // keep the copy in bounds, zero the output
+          bar.bad_block = 1;
+          status_or(p.d_status, PA_STATUS_BAD_BLOCK);
+          phys = 0;
+        }
+        const int row = phys * kBlockSize;
+        tc::tma_load_3d(dst + b * (kBlockSize * 128), tm, 0, g, row, &full[st]);
+        tc::tma_load_3d(dst + kHalf + b * (kBlockSize * 128), tm, 64, g, row, &full[st]);
+      }
+#pragma unroll
+      for (int b = 0; b < kBlocksTile; ++b) ph[b] = phn[b];
+      nb = nbn;
+    }
+  };
+
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ Q and K loads
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_k);
-      tc::prefetch_tmap(&tm_v);
       mbar_arrive_expect_tx(&bar.q_full, 2 * kHalf);
       tc::tma_load_3d(smem + kOffQ, &tm_q, 0, g * G, q0 + tok0, &bar.q_full);
       tc::tma_load_3d(smem + kOffQ + kHalf, &tm_q, 64, g * G, q0 + tok0, &bar.q_full);
-      for (int j = 0; j < n_kt; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait_bounded(&bar.kv_empty[st], ((j >> 1) & 1) ^ 1)) {
-          atomicOr(&bar.abort, 1);
-          break;
-        }
-        const int b0 = j * kBlocksTile;
-        const int nb = min(kBlocksTile, nblk - b0);
-        char* sk = smem + kOffKV + st * kStageBytes;
-        char* sv = sk + 2 * kHalf;
-        mbar_arrive_expect_tx(&bar.kv_full[st], nb * 4 * (kBlockSize * 128));
-        for (int b = 0; b < nb; ++b) {
-          int phys = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + b0 + b];
-          if (phys < 0 || phys >= p.num_blocks) {  // keep the copy in bounds, zero the output
-            bar.bad_block = 1;
-            status_or(p.d_status, PA_STATUS_BAD_BLOCK);
-            phys = 0;
-          }
-          const int row = phys * kBlockSize;
-          const int off = b * kBlockSize * 128;
-          tc::tma_load_3d(sk + off, &tm_k, 0, g, row, &bar.kv_full[st]);
-          tc::tma_load_3d(sk + kHalf + off, &tm_k, 64, g, row, &bar.kv_full[st]);
-          tc::tma_load_3d(sv + off, &tm_v, 0, g, row, &bar.kv_full[st]);
-          tc::tma_load_3d(sv + kHalf + off, &tm_v, 64, g, row, &bar.kv_full[st]);
-        }
-      }
+      produce(&tm_k, kOffK, kKStages, bar.k_full, bar.k_empty);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ V loads
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_v);
+      produce(&tm_v, kOffV, kVStages, bar.v_full, bar.v_empty);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -211,34 +243,41 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const uint32_t id_pv = tc::idesc_bf16_f32(kRowsTile, kD, false, true);
       const uint32_t sQ = smem_addr(smem + kOffQ);
       const uint32_t sP = smem_addr(smem + kOffP);
-      // S(j) = Q K_j^T into TMEM buffer j % 2
+      // S(j) = Q K_j^T into TMEM buffer j % 2; K_j's stage is free when it completes
       auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait_bounded(&bar.kv_full[st], (j >> 1) & 1)) return false;
-        if (!mbar_wait_bounded(&bar.s_empty[st], ((j >> 1) & 1) ^ 1)) return false;
+        const int st = j % kKStages;
+        if (!mbar_wait_bounded(&bar.k_full[st], (j / kKStages) & 1)) return false;
+        if (!mbar_wait_bounded(&bar.s_empty[j & 1], ((j >> 1) & 1) ^ 1)) return false;
         tc::fence_after_sync();
-        const uint32_t sK = smem_addr(smem + kOffKV + st * kStageBytes);
+        const uint32_t sK = smem_addr(smem + kOffK + st * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + kColS0 + st * kKeysTile, tc::smem_desc(sQ + o, 16, 1024),
+          tc::mma_bf16(tmem + kColS0 + (j & 1) * kKeysTile, tc::smem_desc(sQ + o, 16, 1024),
                        tc::smem_desc(sK + o, 16, 1024), id_qk, kk > 0);
         }
-        tc::mma_commit(&bar.s_full[st]);
+        tc::mma_commit(&bar.s_full[j & 1]);
+        tc::mma_commit(&bar.k_empty[st]);
         return true;
       };
       bool ok = mbar_wait_bounded(&bar.q_full, 0);
       if (ok) ok = issue_s(0);
       if (ok && n_kt > 1) ok = issue_s(1);
       for (int j = 0; ok && j < n_kt; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait_bounded(&bar.p_full, j & 1)) {
+        // S(j + 2) runs while the softmax of tile j finishes
+        if (j + 2 < n_kt && !issue_s(j + 2)) {
+          ok = false;
+          break;
+        }
+        const int vs = j % kVStages;
+        if (!mbar_wait_bounded(&bar.p_full, j & 1) ||
+            !mbar_wait_bounded(&bar.v_full[vs], (j / kVStages) & 1)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         // O += P_j V_j (V is MN-major: head_dim contiguous)
-        const uint32_t sV = smem_addr(smem + kOffKV + st * kStageBytes + 2 * kHalf);
+        const uint32_t sV = smem_addr(smem + kOffV + vs * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kKeysTile / 16; ++kk) {
           const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -246,9 +285,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                        tc::smem_desc(sV + kk * (16 * 128), kHalf, 1024), id_pv,
                        (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc::mma_commit(&bar.kv_empty[st]);
+        tc::mma_commit(&bar.v_empty[vs]);
         tc::mma_commit(&bar.pv_done);
-        if (j + 2 < n_kt) ok = issue_s(j + 2);
       }
       if (!ok) atomicOr(&bar.abort, 1);
     }
@@ -256,7 +294,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ------------------------------------------------------------ softmax
     const int quad = warp & 3;                 // TMEM lane quarter this warp may access
     const int r = quad * 32 + lane;            // tile row owned by this thread
-    const int ri = r / G, rh = r % G;          // token within the tile, head within the group
+    const int ri = r / G;                      // token of the row within the tile
     const int pos = ri < ntok ? ctx - q_len + tok0 + ri : -1;  // absolute position (-1: padding row)
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     char* sP = smem + kOffP;
@@ -280,29 +318,72 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.s_empty[buf]);
-      // causal mask over absolute positions, scores in the log2 domain
+      if (lane == 0) mbar_arrive(&bar.s_empty[buf]);  // S(j + 2) may now overwrite the buffer
+      // Tiles entirely below the diagonal need no mask (every key <= every
+      // row's position); the others mask keys past each row's position.
       const int key0 = j * kKeysTile;
-      float mx = -INFINITY;
+      const bool full = key0 + kKeysTile - 1 <= ctx - q_len + tok0 && p.scale_log2 > 0.f;
+      float mx;
+      {
+        float mp[8];
 #pragma unroll
-      for (int c = 0; c < kKeysTile; ++c) {
-        const float v = (key0 + c <= pos) ? sc[c] * p.scale_log2 : -INFINITY;
-        sc[c] = v;
-        mx = fmaxf(mx, v);
+        for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < kKeysTile; ++c) mp[c & 7] = fmaxf(mp[c & 7], sc[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kKeysTile; ++c) {
+            const float v = (key0 + c <= pos) ? sc[c] * p.scale_log2 : -INFINITY;
+            sc[c] = v;
+            mp[c & 7] = fmaxf(mp[c & 7], v);
+          }
+        }
+        mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        if (full) mx *= p.scale_log2;  // scores in the log2 domain
       }
+      // lazy running max: move it only when a score exceeds it by more than 8
+      const bool need = mx > m + 8.f;
+      const bool warp_need = __any_sync(0xffffffffu, need);
+      const float mn = need ? mx : m;
+      const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2(m - mn) : 1.f);
+      m = mn;
+      // P = 2^(s - m) in registers (bf16 pairs) before touching shared P
+      uint32_t pk[kKeysTile / 2];
+      float2 rsp[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rsp[i] = make_float2(0.f, 0.f);
+      if (full) {
+        const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nm = make_float2(-m, -m);
+#pragma unroll
+        for (int c = 0; c < kKeysTile / 2; ++c) {
+          const float2 t = __ffma2_rn(make_float2(sc[2 * c], sc[2 * c + 1]), c2, nm);
+          const float2 w = make_float2(ex2(t.x), ex2(t.y));
+          rsp[c & 3] = __fadd2_rn(rsp[c & 3], w);
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(w.x, w.y);
+          pk[c] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kKeysTile / 2; ++c) {
+          const float a = sc[2 * c], b = sc[2 * c + 1];
+          const float2 w = make_float2(a == -INFINITY ? 0.f : ex2(a - m), b == -INFINITY ? 0.f : ex2(b - m));
+          rsp[c & 3] = __fadd2_rn(rsp[c & 3], w);
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(w.x, w.y);
+          pk[c] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
+      const float rs = ((rsp[0].x + rsp[0].y) + (rsp[1].x + rsp[1].y)) +
+                       ((rsp[2].x + rsp[2].y) + (rsp[3].x + rsp[3].y));
+      l = l * alpha + rs;
       // P_{j-1} V_{j-1} must be complete before O is rescaled or P rewritten
       if (j > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.pv_done, (j - 1) & 1));
         if (!ok) break;
         tc::fence_after_sync();
-      }
-      const bool need = mx > m + 8.f;
-      if (__any_sync(0xffffffffu, need)) {
-        const float mn = need ? mx : m;
-        const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
-        l *= alpha;
-        m = mn;
-        if (j > 0) {  // O holds tiles 0 .. j-1: rescale this warp's rows in TMEM
+        if (warp_need) {  // O holds tiles 0 .. j-1: rescale this warp's rows in TMEM
 #pragma unroll
           for (int c = 0; c < kD / 32; ++c) {
             uint32_t o[32];
@@ -315,33 +396,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tc::tmem_wait_st();
         }
       }
-      // P = 2^(s - m) as bf16 into the 128-byte swizzled P tile (row r)
-      float rs = 0.f;
+      // row r of the 128-byte swizzled P tile (keys 0-63 | 64-127)
 #pragma unroll
-      for (int kc = 0; kc < kKeysTile / 8; ++kc) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = sc[kc * 8 + 2 * e], b = sc[kc * 8 + 2 * e + 1];
-          const float pa = a == -INFINITY ? 0.f : ex2(a - m);
-          const float pb = b == -INFINITY ? 0.f : ex2(b - m);
-          rs += pa + pb;
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
-          w[e] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
+      for (int kc = 0; kc < kKeysTile / 8; ++kc)
         *reinterpret_cast<uint4*>(sP + (kc >> 3) * kHalf + tc::sw128_offset(r, kc & 7)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      l += rs;
+            make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
       // last tile: zero the value rows no key of this CTA may use
       if (j == n_kt - 1) {
-        const int st = j & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.kv_full[st], (j >> 1) & 1));
+        const int vs = j % kVStages;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.v_full[vs], (j / kVStages) & 1));
         if (!ok) break;
         // rows past the context hold stale or poisoned slots; rows past the
         // last loaded block were never written by this CTA
         if (key0 + r >= min(ctx, nblk * kBlockSize)) {
-          char* sv = smem + kOffKV + st * kStageBytes + 2 * kHalf;
+          char* sv = smem + kOffV + vs * kTileBytes;
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -363,7 +431,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
 
   __syncthreads();  // every role done issuing; the last P.V is complete
-  if (warp >= 2) {
+  if (warp >= 2 && warp <= 5) {
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const int ri = r / G, rh = r % G;
@@ -443,7 +511,7 @@ bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid,
 bool tc_supported(const PrefillArgs& a) {
   const int group = a.num_q_heads / a.pool.num_kv_heads;
   return a.pool.dtype == PA_BF16 && a.pool.head_dim == kD && kRowsTile % group == 0 &&
-         group <= 8 && encode_tiled() != nullptr;
+         group <= 8 && a.num_seqs <= kMaxPrefixSeqs && encode_tiled() != nullptr;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
@@ -470,8 +538,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   p.d_status = a.d_status;
   const int tq_tokens = kRowsTile / group;
   const int tiles = (a.num_tokens + tq_tokens - 1) / tq_tokens + a.num_seqs;  // upper bound
-  const int smem = kOffPrefix + (a.num_seqs + 1) * 4 + 1024;
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  const int smem = kSmemTc;
+  if (a.num_seqs > kMaxPrefixSeqs) return cudaErrorInvalidValue;
   cudaError_t err =
       cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
