@@ -90,7 +90,7 @@ struct SmemLayout {
   int tokens_per_unit;  // tokens of one block moved per pipeline stage (16, 8 or 4)
   int parts;            // 16 / tokens_per_unit
   int part_bytes;       // one K (or V) part: tokens_per_unit * Hkv * D * elt
-  int off_bars, off_done, off_flags, off_mbars, off_table, off_merge, off_prefix, total;
+  int off_bars, off_done, off_flags, off_mbars, off_table, off_ntok, off_merge, off_prefix, total;
 };
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -108,7 +108,8 @@ __host__ __device__ inline SmemLayout make_layout(int stages, int tokens_per_uni
   L.off_flags = L.off_done + stages * 4;
   L.off_mbars = align_up(L.off_flags + stages * 4, 16);   // 2 merge mbarriers per KV head
   L.off_table = align_up(L.off_mbars + 2 * hkv * 8, 16);
-  L.off_merge = align_up(L.off_table + kTableCache * 4, 16);
+  L.off_ntok = L.off_table + kTableCache * 4;  // valid tokens of each cached block
+  L.off_merge = align_up(L.off_ntok + kTableCache, 16);
   const int merge_bytes = (wh - 1) * hkv * group * (d + 2) * 4;
   L.off_prefix = align_up(L.off_merge + merge_bytes, 16);
   L.total = align_up(L.off_prefix + (num_seqs + 1) * 4, 128);
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   uint64_t* merge_full = reinterpret_cast<uint64_t*>(smem + L.off_mbars);
   uint64_t* merge_empty = merge_full + HKV;
   int* table = reinterpret_cast<int*>(smem + L.off_table);
+  uint8_t* block_ntok = reinterpret_cast<uint8_t*>(smem + L.off_ntok);
   float* merge = reinterpret_cast<float*>(smem + L.off_merge);
   int* prefix = reinterpret_cast<int*>(smem + L.off_prefix);
   __shared__ int warp_sums[kWarps];
@@ -240,10 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   if (lo >= hi) return;
 
   // stage this CTA's slice of the block tables (first kTableCache blocks)
+  // with the number of context tokens each block holds
   const int n_cached = static_cast<int>(min(hi - lo, static_cast<int64_t>(kTableCache)));
   for (int i = tid; i < n_cached; i += kThreads) {
     const int s = upper_index(prefix, S, lo + i);
-    table[i] = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + (lo + i - prefix[s])];
+    const int j = static_cast<int>(lo + i - prefix[s]);
+    table[i] = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
+    block_ntok[i] = static_cast<uint8_t>(min(kBlockSize, p.context_lens[s] - j * kBlockSize));
   }
   __syncthreads();
 
@@ -255,16 +260,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   // Issue unit u into its stage (called by one lane).
   auto issue = [&](int64_t u) {
     const int st = static_cast<int>(u % L.stages);
-    const int64_t blk = lo + u / parts;
+    const int64_t rel = u / parts;  // block of the CTA's range
     const int part = static_cast<int>(u % parts);
-    const int s = upper_index(prefix, S, blk);
-    const int j = static_cast<int>(blk - prefix[s]);  // logical block of sequence s
-    const int ctx = p.context_lens[s];
-    const int64_t rel = blk - lo;
-    const int phys = rel < kTableCache ? table[rel]
-                                       : p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
-    const int first_tok = j * kBlockSize + part * tpu;
-    const int ntok = min(tpu, ctx - first_tok);
+    int phys, block_tokens;
+    if (rel < kTableCache) {
+      phys = table[rel];
+      block_tokens = block_ntok[rel];
+    } else {
+      const int s = upper_index(prefix, S, lo + rel);
+      const int j = static_cast<int>(lo + rel - prefix[s]);  // logical block of sequence s
+      phys = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
+      block_tokens = min(kBlockSize, p.context_lens[s] - j * kBlockSize);
+    }
+    const int ntok = min(tpu, block_tokens - part * tpu);
     if (phys < 0 || phys >= p.num_blocks) {
       flags[st] = -1;
       status_or(p.d_status, PA_STATUS_BAD_BLOCK);
@@ -587,12 +595,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 
 // Merge the partials of sequences that straddle CTAs: o = sum_c a_c acc_c /
 // sum_c a_c l_c with a_c = 2^(m_c - max_c m_c). One warp per (sequence,
-// head); partials are read four at a time so their loads overlap.
+// head), eight per CTA, so every partial of the batch is read at once;
+// partials are read four at a time so their loads overlap.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p, int grid) {
   pdl_wait_primary();
   constexpr int kPer = D / 32;  // elements per lane
-  const int s = blockIdx.x;
+  const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (item >= p.num_seqs * p.hq) return;
+  const int s = item / p.hq, h = item % p.hq;
+  const int lane = threadIdx.x & 31;
   const int* prefix = p.ws_prefix;
   const int64_t B = prefix[p.num_seqs];
   const int64_t a0 = prefix[s], a1 = prefix[s + 1];
@@ -601,51 +613,46 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
   const int64_t c_first = ((a0 + 1) * grid - 1) / B;
   const int64_t c_last = (a1 * grid - 1) / B;
   if (c_first == c_last) return;  // finished by the decode kernel
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = query_row(p, s);
-  T* orow = static_cast<T*>(p.out) + static_cast<int64_t>(row) * p.hq * D;
-  for (int h = warp; h < p.hq; h += blockDim.x >> 5) {
-    float m = -INFINITY, l = 0.f;
-    float acc[kPer];
+  float m = -INFINITY, l = 0.f;
+  float acc[kPer];
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    bool poisoned = false;
-    for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
-      float2 ml[4];
-      float v[4][kPer];
-      bool use[4];
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  bool poisoned = false;
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+    float2 ml[4];
+    float v[4][kPer];
+    bool use[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t c = c0 + j;
-        use[j] = c <= c_last && (c * B / grid != (c + 1) * B / grid);
-        if (use[j]) {
-          ml[j] = p.ws_ml[(c + s) * p.hq + h];
-          const float* src = p.ws_acc + ((c + s) * p.hq + h) * D + lane * kPer;
+    for (int j = 0; j < 4; ++j) {
+      const int64_t c = c0 + j;
+      use[j] = c <= c_last && (c * B / grid != (c + 1) * B / grid);
+      if (use[j]) {
+        ml[j] = p.ws_ml[(c + s) * p.hq + h];
+        const float* src = p.ws_acc + ((c + s) * p.hq + h) * D + lane * kPer;
 #pragma unroll
-          for (int e = 0; e < kPer; e += 2) {
-            const float2 x = *reinterpret_cast<const float2*>(src + e);
-            v[j][e] = x.x;
-            v[j][e + 1] = x.y;
-          }
+        for (int e = 0; e < kPer; e += 2) {
+          const float2 x = *reinterpret_cast<const float2*>(src + e);
+          v[j][e] = x.x;
+          v[j][e + 1] = x.y;
         }
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (!use[j]) continue;
-        poisoned |= ml[j].y < 0.f;
-        const float mn = fmaxf(m, ml[j].x);
-        const float a = merge_factor(m, mn), b = merge_factor(ml[j].x, mn);
-        l = l * a + ml[j].y * b;
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) acc[e] = acc[e] * a + v[j][e] * b;
-        m = mn;
-      }
     }
-    const float inv = poisoned ? 0.f : 1.f / l;
-    T* dst = orow + h * D + lane * kPer;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) dst[e] = from_float<T>(acc[e] * inv);
+    for (int j = 0; j < 4; ++j) {
+      if (!use[j]) continue;
+      poisoned |= ml[j].y < 0.f;
+      const float mn = fmaxf(m, ml[j].x);
+      const float a = merge_factor(m, mn), b = merge_factor(ml[j].x, mn);
+      l = l * a + ml[j].y * b;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) acc[e] = acc[e] * a + v[j][e] * b;
+      m = mn;
+    }
   }
+  const float inv = poisoned ? 0.f : 1.f / l;
+  T* dst = static_cast<T*>(p.out) + (static_cast<int64_t>(query_row(p, s)) * p.hq + h) * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) dst[e] = from_float<T>(acc[e] * inv);
 }
 
 template <typename T, int D, int G, int WH>
@@ -699,7 +706,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   // merge kernel, launched with programmatic stream serialization so its
   // launch overlaps the decode kernel's tail (it waits with griddepcontrol.wait)
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.num_seqs);
+  cfg.gridDim = dim3((a.num_seqs * a.num_q_heads + 7) / 8);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
