@@ -36,10 +36,11 @@ MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# DRAM bytes (read + write) of one pa_decode call on the decode batch, from an
-# ncu capture (profiles/decode_b64_bf16.md), valid for the kernel source whose
-# sha256 prefix is given; null once the source changes.
-NCU_DECODE_TRAFFIC = {"bytes": None, "src_sha": None}
+# DRAM bytes (read + write) of one pa_decode call (decode_kernel +
+# decode_reduce_kernel) on the decode batch, from an ncu capture
+# (profiles/decode_b64_bf16.md), valid for the kernel source whose sha256
+# prefix is given; reported as null once the source changes.
+NCU_DECODE_TRAFFIC = {"bytes": 642085120, "src_sha": "6a5da8d1ebe07ed5"}
 
 
 def _src_sha(path: str) -> str:
@@ -256,7 +257,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
 
     pk = peaks()
     decode_gbs = nb["decode"] / (decode_ms * 1e-3) / 1e9
-    src = os.path.join(ROOT, "paged_kv_cache_176_gb300", "csrc", "decode.cu")
+    src = os.path.join(ROOT, "paged_kv_cache_176_gb300", "csrc", "decode_impl.cuh")
     traffic = None
     if NCU_DECODE_TRAFFIC["bytes"] and NCU_DECODE_TRAFFIC["src_sha"] == _src_sha(src):
         traffic = NCU_DECODE_TRAFFIC["bytes"]
