@@ -118,6 +118,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of ``x`` over all ranks (``x`` itself without a process
+    group). Used for the timed region: the job is as slow as its slowest rank."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def step_bytes(w) -> dict:
     """Algorithmic HBM bytes of one decode step (KV write + decode)."""
     elt = w.k_pool.element_size()
@@ -210,11 +222,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     t1.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1) / args.steps
-    if dist:
-        tm = torch.tensor([ms], dtype=torch.float64, device=dev)
-        tdist.all_reduce(tm, op=tdist.ReduceOp.MAX)
-        ms = float(tm.item())
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, dev)
 
     # end to end through the public API with host buffers
     pin = {k: t.pin_memory() for k, t in (("q", w.q), ("k_new", w.k_new), ("v_new", w.v_new),
@@ -248,7 +256,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         e1.record(stream)
         torch.cuda.synchronize(dev)
         wall = (time.perf_counter() - wall0) / e2e_steps * 1e3
-    e2e_ms = max(e0.elapsed_time(e1) / e2e_steps, wall)
+    e2e_ms = max_over_ranks(max(e0.elapsed_time(e1) / e2e_steps, wall), dev)
 
     # mixed step (secondary measurement)
     mixed = None
