@@ -43,7 +43,8 @@ constexpr int kD = 128;              // head_dim of the tensor-core path
 constexpr int kRowsTile = 128;       // query rows per CTA (MMA M)
 constexpr int kKeysTile = 128;       // keys per tile (MMA N of Q K^T)
 constexpr int kBlocksTile = kKeysTile / kBlockSize;
-constexpr int kThreadsTc = 224;      // warp 0 K loads, warp 1 MMA, warps 2-5 softmax, warp 6 V loads
+constexpr int kThreadsTc = 352;      // warp 0 K loads, warp 1 MMA, warps 2-9 softmax, warp 10 V loads
+constexpr int kVWarp = 10;
 constexpr int kHalf = 16384;         // one 64-column half of a 128-row bf16 tile
 constexpr int kTileBytes = 2 * kHalf;
 constexpr int kKStages = 3;          // K is released as soon as S = Q K^T is done
@@ -61,7 +62,7 @@ constexpr int kMaxPrefixSeqs = kTileBytes / 4 - 1;
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0;     // S buffers at 0 and 128
-constexpr uint32_t kColO = 256;    // O accumulator
+constexpr uint32_t kColO = 256;    // O accumulators: keys 0-63 of every tile at 256, keys 64-127 at 384
 
 struct TcParams {
   const int32_t* cu_q_lens;
@@ -82,7 +83,7 @@ struct TcBarriers {
   uint64_t v_empty[kVStages];
   uint64_t s_full[2];
   uint64_t s_empty[2];
-  uint64_t p_full;
+  uint64_t p_full[2][2];  // [S buffer][key half]: P of one 64-key half written
   uint64_t pv_done;
   uint32_t tmem_base;
   int bad_block;
@@ -162,9 +163,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.s_full[i], 1);
-      mbar_init(&bar.s_empty[i], 4);
+      mbar_init(&bar.s_empty[i], 8);
     }
-    mbar_init(&bar.p_full, 4);
+    for (int b = 0; b < 2; ++b)
+      for (int h = 0; h < 2; ++h) mbar_init(&bar.p_full[b][h], 4);
     mbar_init(&bar.pv_done, 1);
     bar.bad_block = 0;
     bar.abort = 0;
@@ -178,7 +180,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = bar.tmem_base;
-  float row_sum = 0.f;  // softmax threads: sum of the row's weights
 
   // Block-table entries of key tile j, read as one batch of independent loads.
   auto tile_blocks = [&](int j, int (&ph)[kBlocksTile]) -> int {
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tc::tma_load_3d(smem + kOffQ + kHalf, &tm_q, 64, g * G, q0 + tok0, &bar.q_full);
       produce(&tm_k, kOffK, kKStages, bar.k_full, bar.k_empty);
     }
-  } else if (warp == 6) {
+  } else if (warp == kVWarp) {
     // ------------------------------------------------------------ V loads
     if (lane == 0) {
       tc::prefetch_tmap(&tm_v);
@@ -247,7 +248,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       auto issue_s = [&](int j) -> bool {
         const int st = j % kKStages;
         if (!mbar_wait_bounded(&bar.k_full[st], (j / kKStages) & 1)) return false;
-        if (!mbar_wait_bounded(&bar.s_empty[j & 1], ((j >> 1) & 1) ^ 1)) return false;
         tc::fence_after_sync();
         const uint32_t sK = smem_addr(smem + kOffK + st * kTileBytes);
 #pragma unroll
@@ -264,65 +264,76 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (ok) ok = issue_s(0);
       if (ok && n_kt > 1) ok = issue_s(1);
       for (int j = 0; ok && j < n_kt; ++j) {
-        // S(j + 2) runs while the softmax of tile j finishes
+        const int vs = j % kVStages;
+        if (!mbar_wait_bounded(&bar.v_full[vs], (j / kVStages) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sV = smem_addr(smem + kOffV + vs * kTileBytes);
+        // O_h += P_h V_h for the two 64-key halves, each as soon as its P is
+        // in TMEM (P_h sits in the first 32 columns of S_j's h-th half)
+        for (int h = 0; h < 2 && ok; ++h) {
+          // one barrier pair per S buffer: the next arrival on it needs
+          // S(j + 2), which is issued only after this wait
+          if (!mbar_wait_bounded(&bar.p_full[j & 1][h], (j >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t pcol = tmem + kColS0 + (j & 1) * kKeysTile + h * (kKeysTile / 2);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16_ts(tmem + kColO + h * kD, pcol + kk * 8,
+                            tc::smem_desc(sV + (4 * h + kk) * (16 * 128), kHalf, 1024), id_pv,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        tc::mma_commit(&bar.v_empty[vs]);
+        tc::mma_commit(&bar.pv_done);
+        // S(j + 2) reuses S_j's columns: the tensor pipe runs it after P_j V_j
         if (j + 2 < n_kt && !issue_s(j + 2)) {
           ok = false;
           break;
         }
-        const int vs = j % kVStages;
-        if (!mbar_wait_bounded(&bar.p_full, j & 1) ||
-            !mbar_wait_bounded(&bar.v_full[vs], (j / kVStages) & 1)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        // O += P_j V_j (V is MN-major: head_dim contiguous)
-        const uint32_t sV = smem_addr(smem + kOffV + vs * kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < kKeysTile / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + kColO, tc::smem_desc(sP + o, 16, 1024),
-                       tc::smem_desc(sV + kk * (16 * 128), kHalf, 1024), id_pv,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc::mma_commit(&bar.v_empty[vs]);
-        tc::mma_commit(&bar.pv_done);
       }
       if (!ok) atomicOr(&bar.abort, 1);
     }
   } else {
     // ------------------------------------------------------------ softmax
+    // Two threads per query row: half hf owns keys 64*hf .. 64*hf+63 of every
+    // tile and runs its own online softmax into its own O accumulator; the
+    // two (max, sum, O) triples are merged once, in the epilogue.
     const int quad = warp & 3;                 // TMEM lane quarter this warp may access
+    const int hf = (warp - 2) >> 2;            // key half
     const int r = quad * 32 + lane;            // tile row owned by this thread
     const int ri = r / G;                      // token of the row within the tile
     const int pos = ri < ntok ? ctx - q_len + tok0 + ri : -1;  // absolute position (-1: padding row)
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    char* sP = smem + kOffP;
+    const uint32_t ocol = kColO + hf * kD;     // this half's O accumulator
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    constexpr int kCols = kKeysTile / 2;
     for (int j = 0; j < n_kt; ++j) {
       const int buf = j & 1;
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.s_full[buf], (j >> 1) & 1));
       if (!ok) break;
       tc::fence_after_sync();
-      float sc[kKeysTile];
+      float sc[kCols];
       {
-        uint32_t raw[4][32];
+        uint32_t raw[2][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tc::tmem_ld32(trow + kColS0 + buf * kKeysTile + c * 32, raw[c]);
+        for (int c = 0; c < 2; ++c)
+          tc::tmem_ld32(trow + kColS0 + buf * kKeysTile + hf * kCols + c * 32, raw[c]);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) sc[c * 32 + e] = __uint_as_float(raw[c][e]);
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.s_empty[buf]);  // S(j + 2) may now overwrite the buffer
-      // Tiles entirely below the diagonal need no mask (every key <= every
-      // row's position); the others mask keys past each row's position.
-      const int key0 = j * kKeysTile;
-      const bool full = key0 + kKeysTile - 1 <= ctx - q_len + tok0 && p.scale_log2 > 0.f;
+      // Key halves entirely below the diagonal need no mask (every key <=
+      // every row's position); the others mask keys past each row's position.
+      const int key0 = j * kKeysTile + hf * kCols;
+      const bool full = key0 + kCols - 1 <= ctx - q_len + tok0 && p.scale_log2 > 0.f;
       float mx;
       {
         float mp[8];
@@ -330,10 +341,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
         if (full) {
 #pragma unroll
-          for (int c = 0; c < kKeysTile; ++c) mp[c & 7] = fmaxf(mp[c & 7], sc[c]);
+          for (int c = 0; c < kCols; ++c) mp[c & 7] = fmaxf(mp[c & 7], sc[c]);
         } else {
 #pragma unroll
-          for (int c = 0; c < kKeysTile; ++c) {
+          for (int c = 0; c < kCols; ++c) {
             const float v = (key0 + c <= pos) ? sc[c] * p.scale_log2 : -INFINITY;
             sc[c] = v;
             mp[c & 7] = fmaxf(mp[c & 7], v);
@@ -350,7 +361,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2(m - mn) : 1.f);
       m = mn;
       // P = 2^(s - m) in registers (bf16 pairs) before touching shared P
-      uint32_t pk[kKeysTile / 2];
+      uint32_t pk[kCols / 2];
       float2 rsp[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) rsp[i] = make_float2(0.f, 0.f);
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 nm = make_float2(-m, -m);
 #pragma unroll
-        for (int c = 0; c < kKeysTile / 2; ++c) {
+        for (int c = 0; c < kCols / 2; ++c) {
           const float2 t = __ffma2_rn(make_float2(sc[2 * c], sc[2 * c + 1]), c2, nm);
           const float2 w = make_float2(ex2(t.x), ex2(t.y));
           rsp[c & 3] = __fadd2_rn(rsp[c & 3], w);
@@ -367,7 +378,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kKeysTile / 2; ++c) {
+        for (int c = 0; c < kCols / 2; ++c) {
           const float a = sc[2 * c], b = sc[2 * c + 1];
           const float2 w = make_float2(a == -INFINITY ? 0.f : ex2(a - m), b == -INFINITY ? 0.f : ex2(b - m));
           rsp[c & 3] = __fadd2_rn(rsp[c & 3], w);
@@ -378,88 +389,99 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const float rs = ((rsp[0].x + rsp[0].y) + (rsp[1].x + rsp[1].y)) +
                        ((rsp[2].x + rsp[2].y) + (rsp[3].x + rsp[3].y));
       l = l * alpha + rs;
-      // P_{j-1} V_{j-1} must be complete before O is rescaled or P rewritten
-      if (j > 0) {
+      // O_hf holds tiles 0 .. j-1 once P_{j-1} V_{j-1} is complete: rescale
+      // this warp's rows only when its running max moved
+      if (j > 0 && warp_need) {
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.pv_done, (j - 1) & 1));
         if (!ok) break;
         tc::fence_after_sync();
-        if (warp_need) {  // O holds tiles 0 .. j-1: rescale this warp's rows in TMEM
 #pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
-            uint32_t o[32];
-            tc::tmem_ld32(trow + kColO + c * 32, o);
-            tc::tmem_wait_ld();
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(trow + ocol + c * 32, o);
+          tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc::tmem_st32(trow + kColO + c * 32, o);
-          }
-          tc::tmem_wait_st();
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc::tmem_st32(trow + ocol + c * 32, o);
         }
       }
-      // row r of the 128-byte swizzled P tile (keys 0-63 | 64-127)
-#pragma unroll
-      for (int kc = 0; kc < kKeysTile / 8; ++kc)
-        *reinterpret_cast<uint4*>(sP + (kc >> 3) * kHalf + tc::sw128_offset(r, kc & 7)) =
-            make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
-      // last tile: zero the value rows no key of this CTA may use
+      // P (bf16 pairs) over the first 32 columns of this half's S columns
+      tc::tmem_st32(trow + kColS0 + buf * kKeysTile + hf * kCols, pk);
+      tc::tmem_wait_st();
+      // last tile: zero the value rows no key of this CTA may use (this half
+      // zeroes head_dim columns 64*hf .. 64*hf+63 of row r)
       if (j == n_kt - 1) {
         const int vs = j % kVStages;
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.v_full[vs], (j / kVStages) & 1));
         if (!ok) break;
         // rows past the context hold stale or poisoned slots; rows past the
         // last loaded block were never written by this CTA
-        if (key0 + r >= min(ctx, nblk * kBlockSize)) {
-          char* sv = smem + kOffV + vs * kTileBytes;
+        if (j * kKeysTile + r >= min(ctx, nblk * kBlockSize)) {
+          char* sv = smem + kOffV + vs * kTileBytes + hf * kHalf;
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(sv + h * kHalf + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(sv + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      fence_proxy_async_smem();  // P (and zeroed V rows) visible to the tensor cores
+      fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.p_full);
+      if (lane == 0) mbar_arrive(&bar.p_full[buf][hf]);
     }
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.pv_done, (n_kt - 1) & 1));
       if (ok) tc::fence_after_sync();
     }
     if (!ok) atomicOr(&bar.abort, 1);
-    row_sum = l;
+    // this half's (max, sum) for the epilogue merge; the P tile is free now
+    float* ml = reinterpret_cast<float*>(smem + kOffP);
+    ml[(hf * kRowsTile + r) * 2] = m;
+    ml[(hf * kRowsTile + r) * 2 + 1] = l;
   }
 
   __syncthreads();  // every role done issuing; the last P.V is complete
-  if (warp >= 2 && warp <= 5) {
+  if (warp >= 2 && warp < kVWarp) {
     const int quad = warp & 3;
+    const int hf = (warp - 2) >> 2;  // this thread writes head_dim columns 64*hf .. 64*hf+63
     const int r = quad * 32 + lane;
     const int ri = r / G, rh = r % G;
     if (bar.abort == 0) {
-      // epilogue: O / l as bf16 (every lane loads: tcgen05.ld is warp-collective)
+      // epilogue: merge the two key halves, O = (a0 O0 + a1 O1) / (a0 l0 + a1 l1)
       const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-      uint32_t raw[4][32];
+      uint32_t raw[2][2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(trow + kColO + c * 32, raw[c]);
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) tc::tmem_ld32(trow + kColO + h * kD + hf * 64 + c * 32, raw[h][c]);
       tc::tmem_wait_ld();
       if (ri < ntok) {
-        const float inv = bar.bad_block ? 0.f : 1.f / row_sum;
-        __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + tok0 + ri) * p.hq + g * G + rh) * kD;
+        const float* ml = reinterpret_cast<const float*>(smem + kOffP);
+        const float m0 = ml[r * 2], l0 = ml[r * 2 + 1];
+        const float m1 = ml[(kRowsTile + r) * 2], l1 = ml[(kRowsTile + r) * 2 + 1];
+        const float mm = fmaxf(m0, m1);
+        const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mm);
+        const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mm);
+        const float inv = bar.bad_block ? 0.f : 1.f / (a0 * l0 + a1 * l1);
+        const float s0 = a0 * inv, s1 = a1 * inv;
+        __nv_bfloat16* orow =
+            out + (static_cast<int64_t>(q0 + tok0 + ri) * p.hq + g * G + rh) * kD + hf * 64;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint32_t w[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(raw[c][e + 2 * k]) * inv,
-                                                              __uint_as_float(raw[c][e + 2 * k + 1]) * inv);
+              const int i0 = e + 2 * k;
+              const float x0 = __uint_as_float(raw[0][c][i0]) * s0 + __uint_as_float(raw[1][c][i0]) * s1;
+              const float x1 = __uint_as_float(raw[0][c][i0 + 1]) * s0 + __uint_as_float(raw[1][c][i0 + 1]) * s1;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
               w[k] = *reinterpret_cast<const uint32_t*>(&h2);
             }
             *reinterpret_cast<uint4*>(orow + c * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
           }
       }
-    } else if (r == 0) {
+    } else if (r == 0 && hf == 0) {
       status_or(p.d_status, PA_STATUS_TIMEOUT);
     }
   }
