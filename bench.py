@@ -262,6 +262,16 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     mixed = None
     if not args.skip_mixed:
         mixed = run_mixed(args, dev, stream)
+    extra = None
+    if not args.skip_extra:
+        extra = [
+            run_decode_workload("wide_gqa_decode_bf16: 58 seqs x 4096, 16/4 heads, d 256, pool 23305",
+                                W.wide_gqa_decode(seed=args.seed), dev, stream),
+            run_decode_workload("shared_prefix_decode_bf16: 256 requests x 3 replies, 1000-token "
+                                "shared prefix + 100 unique, replies U[22,356], 32/8 heads, d 128, "
+                                "+ KV write of 768 tokens",
+                                W.shared_prefix_decode(seed=args.seed), dev, stream),
+        ]
 
     pk = peaks()
     decode_gbs = nb["decode"] / (decode_ms * 1e-3) / 1e9
@@ -302,6 +312,64 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     }
     if mixed is not None:
         res["mixed_step"] = mixed
+    if extra is not None:
+        res["other_decode_workloads"] = extra
+    return res
+
+
+def run_decode_workload(name: str, w, dev, stream, reps: int = 30) -> dict:
+    """One decode step (KV write when the workload has one, then pa_decode) on
+    another workload, timed with CUDA events on its stream; GB/s over the
+    logical K/V bytes (every sequence's context) and over the unique bytes
+    (each physical block's filled slots counted once: shared prefix pages are
+    read from L2 after their first use)."""
+    import torch
+    import paged_kv_cache_176_gb300 as pa
+
+    tok = 2 * w.num_kv_heads * w.head_dim * w.k_pool.element_size()
+    ctx = w.context_lens.tolist()
+    bt = w.block_tables.tolist()
+    filled = {}
+    for s, c in enumerate(ctx):
+        for j in range((c + 15) // 16):
+            filled[bt[s][j]] = max(filled.get(bt[s][j], 0), min(16, c - 16 * j))
+    logical = sum(ctx) * tok
+    unique = sum(filled.values()) * tok
+    with torch.cuda.stream(stream):
+        d = {k: (None if getattr(w, k) is None else getattr(w, k).to(dev))
+             for k in ("k_pool", "v_pool", "q", "context_lens", "block_tables", "k_new", "v_new",
+                       "slot_mapping")}
+        out = torch.empty_like(d["q"])
+        ws = torch.empty(pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.head_dim,
+                                                     w.max_blocks_per_seq),
+                         dtype=torch.uint8, device=dev)
+
+    def step():
+        if d["slot_mapping"] is not None:
+            pa.pa_reshape_and_cache(d["k_pool"], d["v_pool"], d["k_new"], d["v_new"],
+                                    d["slot_mapping"], stream=stream)
+        pa.pa_decode(out, d["q"], d["k_pool"], d["v_pool"], d["block_tables"], d["context_lens"],
+                     w.scale, workspace=ws, stream=stream)
+
+    for _ in range(5):
+        step()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / reps
+    pk = peaks()
+    res = {"workload": name, "ms_per_step": round(ms, 4),
+           "logical_kv_gbs": round(logical / (ms * 1e-3) / 1e9, 1),
+           "unique_kv_gbs": round(unique / (ms * 1e-3) / 1e9, 1),
+           "unique_hbm_frac": round(unique / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+           "logical_kv_bytes": logical, "unique_kv_bytes": unique,
+           "attention_tokens_per_s": round(w.num_seqs / (ms * 1e-3), 1)}
+    del d, out, ws
+    torch.cuda.empty_cache()
     return res
 
 
@@ -470,6 +538,8 @@ def main() -> None:
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--mixed-steps", type=int, default=200)
     ap.add_argument("--skip-mixed", action="store_true")
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="skip the wide-head GQA and shared-prefix decode measurements")
     ap.add_argument("--only-mixed", action="store_true",
                     help="run only the mixed step (profiling); prints its measurement")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
