@@ -12,19 +12,25 @@
 // GB300 design (one CTA per 128 query rows of one KV head):
 //  * The 128 rows are 128/G tokens x the G query heads that share the KV head,
 //    so one K/V tile in shared memory serves the whole GQA group.
-//  * Warp 0 moves data with TMA: the Q tile once, then K/V tiles of 128 keys
-//    (8 pool blocks) into a two-stage ring; each block is one 3-D tiled copy
-//    (64 head-dim columns x 16 tokens, 128-byte swizzle) straight out of the
-//    paged pool, so the gather costs no extra pass.
+//  * Warp 0 moves Q once and then K tiles of 128 keys (8 pool blocks) into a
+//    three-stage ring, warp 10 moves V tiles into a two-stage ring; each block
+//    is one 3-D tiled TMA copy (64 head-dim columns x 16 tokens, 128-byte
+//    swizzle) straight out of the paged pool, so the gather costs no extra pass.
 //  * Warp 1 owns 512 TMEM columns and issues the MMAs from one thread:
-//    S = Q K^T (128 x 128, fp32, double-buffered in TMEM) and O += P V
-//    (128 x head_dim, fp32 in TMEM), with tcgen05.commit signalling mbarriers.
-//  * Warps 2-5 hold one query row per thread: they read S from TMEM, apply the
-//    causal mask and the online softmax in the log2 domain, write P as bf16
-//    into shared memory for the P.V MMA, and rescale O in TMEM only when the
-//    row max grows by more than 8 (lazy rescaling). Masked keys get weight 0.
-//  * Value rows past the context in the last key tile are zeroed before the
-//    P.V MMA, so stale or NaN pool slots never reach the result.
+//    S = Q K^T (128 x 128, fp32, double-buffered in TMEM) and, per key half,
+//    O_h += P_h V_h with P_h read from TMEM (the A operand of a TS-MMA) and
+//    V_h (64 keys x head_dim) from shared memory; tcgen05.commit signals
+//    the mbarriers.
+//  * Warps 2-9 hold two threads per query row, one per half of the key tile.
+//    Each reads its 64 S columns from TMEM, applies the causal mask and the
+//    online softmax in the log2 domain with its own (max, sum), writes P as
+//    bf16 pairs back into the S columns it read, and rescales its own O_h only
+//    when its max grows by more than 8 (lazy rescaling). Masked keys get
+//    weight 0. The epilogue merges the two halves' (max, sum, O_h).
+//  * On the last key tile each half zeroes the value rows of its own 64 keys
+//    that lie past the context or past the loaded blocks, before it hands P_h
+//    to the MMA that reads exactly those rows, so stale or NaN slots never
+//    reach the result.
 //  * Every wait is bounded; a timeout sets PA_STATUS_TIMEOUT and the CTA
 //    leaves after releasing its TMEM.
 #include <cuda.h>
@@ -408,19 +414,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // P (bf16 pairs) over the first 32 columns of this half's S columns
       tc::tmem_st32(trow + kColS0 + buf * kKeysTile + hf * kCols, pk);
       tc::tmem_wait_st();
-      // last tile: zero the value rows no key of this CTA may use (this half
-      // zeroes head_dim columns 64*hf .. 64*hf+63 of row r)
+      // last tile: zero the value rows no key of this CTA may use. O_h += P_h V_h
+      // reads keys 64*hf .. 64*hf+63 over all head_dim columns, so the 128
+      // threads of this half clear exactly those rows (thread r: key
+      // 64*hf + r/2, head_dim columns 64*(r&1) .. +63) before they arrive
+      // on p_full[buf][hf].
       if (j == n_kt - 1) {
         const int vs = j % kVStages;
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.v_full[vs], (j / kVStages) & 1));
         if (!ok) break;
         // rows past the context hold stale or poisoned slots; rows past the
         // last loaded block were never written by this CTA
-        if (j * kKeysTile + r >= min(ctx, nblk * kBlockSize)) {
-          char* sv = smem + kOffV + vs * kTileBytes + hf * kHalf;
+        const int kr = hf * (kKeysTile / 2) + (r >> 1);
+        if (j * kKeysTile + kr >= min(ctx, nblk * kBlockSize)) {
+          char* sv = smem + kOffV + vs * kTileBytes + (r & 1) * kHalf;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(sv + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sv + kr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
