@@ -1,0 +1,130 @@
+/*
+ * pa_serving.h -- host-side block manager and iteration-level scheduler that
+ * drive the paged-attention kernels of pa.h.
+ *
+ * Block manager ("vLLM serving internals", PagedAttention as a virtual memory
+ * system): the KV pool is a set of fixed-size physical blocks; each sequence
+ * owns a block table; a block is appended when a sequence outgrows its last
+ * block and returned to the pool when the sequence is released, so at most
+ * block_size - 1 slots of a sequence are ever unused and there is no external
+ * fragmentation ("C13 L2 serving", the waste bound of paging). Blocks are
+ * reference counted: a forked sequence (parallel sampling, beam search)
+ * shares every block of its parent, and the first write into a shared,
+ * partially filled block copies it first (copy-on-write: "C13 L2 serving",
+ * parallel sampling; "Inference engine core techniques", section 1.5).
+ *
+ * Scheduler (the scheduler loop of "vLLM serving internals"; "Inference engine
+ * core techniques", section 2.3; the token budget of the "Chunked Prefill"
+ * page): every step removes finished sequences and releases their blocks,
+ * admits waiting requests while their blocks fit, schedules one token for
+ * every running decode first and then fills the rest of the token budget with
+ * prefill chunks of at most chunk_size tokens. Admission reserves the blocks
+ * a request can reach (prompt + max_new_tokens), so a running sequence never
+ * runs out of blocks (no preemption).
+ *
+ * All functions are host-only and allocate host memory only. An object is
+ * not thread safe; distinct objects are independent. Return values are
+ * pa_status codes (pa.h) unless stated otherwise; PA_ENOSPACE (-6) means the
+ * pool has too few free blocks and nothing was changed.
+ */
+#ifndef PA_SERVING_H
+#define PA_SERVING_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ENOSPACE (-6)
+
+typedef struct pa_block_manager pa_block_manager;
+typedef struct pa_scheduler pa_scheduler;
+
+/* A pool of num_blocks blocks of block_size tokens; NULL on bad sizes. */
+PA_API pa_block_manager* pa_bm_create(int64_t num_blocks, int block_size);
+PA_API void pa_bm_destroy(pa_block_manager* bm);
+PA_API int64_t pa_bm_num_free(const pa_block_manager* bm);
+
+/* Register an empty sequence (PA_EINVAL if the id exists). */
+PA_API int pa_bm_add(pa_block_manager* bm, int64_t seq);
+
+/* child shares every block of parent (reference counts + 1). */
+PA_API int pa_bm_fork(pa_block_manager* bm, int64_t parent, int64_t child);
+
+/*
+ * Reserve slots for n new tokens of seq. slots_out[i] receives the pool slot
+ * (block * block_size + offset) of the i-th new token. If the last block is
+ * shared and partially filled it is first replaced by a fresh copy: the
+ * (source, destination) block pair is written to cow_src/cow_dst (capacity 1
+ * is enough) and *n_cow is set to the number of pairs; the caller copies the
+ * block on the device (pa_copy_blocks) before writing the new tokens.
+ */
+PA_API int pa_bm_append(pa_block_manager* bm, int64_t seq, int n, int64_t* slots_out,
+                        int32_t* cow_src, int32_t* cow_dst, int* n_cow);
+
+/* Release seq: blocks whose count reaches zero return to the pool. */
+PA_API int pa_bm_free(pa_block_manager* bm, int64_t seq);
+
+/* Tokens held by seq (-1 if unknown). */
+PA_API int64_t pa_bm_num_tokens(const pa_block_manager* bm, int64_t seq);
+
+/* Writes seq's block table (at most max_blocks entries); returns its length
+ * or a negative status. */
+PA_API int pa_bm_block_table(const pa_block_manager* bm, int64_t seq, int32_t* out, int max_blocks);
+
+/* Reference count of a physical block (-1 if out of range). */
+PA_API int pa_bm_refcount(const pa_block_manager* bm, int32_t block);
+
+/* A scheduler over bm: token_budget tokens per step, prefill chunks of at
+ * most chunk_size tokens, at most max_running sequences. */
+PA_API pa_scheduler* pa_sched_create(pa_block_manager* bm, int token_budget, int chunk_size,
+                                     int max_running);
+PA_API void pa_sched_destroy(pa_scheduler* s);
+
+/* Queue a request (FIFO): prompt_len >= 1 prompt tokens, then max_new_tokens
+ * generated tokens (>= 1). PA_EINVAL on a duplicate id or bad lengths. */
+PA_API int pa_sched_submit(pa_scheduler* s, int64_t req_id, int prompt_len, int max_new_tokens);
+
+/* One step's batch, in caller-owned host buffers of the stated capacities.
+ * Sequences are ordered decode first (q_len 1), then prefill chunks. */
+typedef struct {
+  int max_seqs, max_tokens, max_blocks_per_seq, max_cow; /* capacities (in) */
+  int num_seqs, num_tokens, num_decode, num_cow;         /* counts (out) */
+  int64_t* seq_ids;       /* [max_seqs] */
+  int32_t* cu_q_lens;     /* [max_seqs + 1] */
+  int32_t* context_lens;  /* [max_seqs], including this step's tokens */
+  int32_t* block_tables;  /* [max_seqs * max_blocks_per_seq], -1 padded */
+  int64_t* slot_mapping;  /* [max_tokens] */
+  int32_t* cow_src;       /* [max_cow] blocks to copy before the KV write */
+  int32_t* cow_dst;       /* [max_cow] */
+} pa_step_plan;
+
+/* Build the next step (removing finished sequences, admitting requests,
+ * reserving slots). Returns PA_OK with num_seqs == 0 when nothing is left
+ * to run, PA_EINVAL if a capacity is too small (finished sequences are still
+ * released and waiting ones admitted, but no slot is reserved). */
+PA_API int pa_sched_step(pa_scheduler* s, pa_step_plan* plan);
+
+/* Mark the last planned step as executed: prefill progress advances; a
+ * decode step, and the step that finishes a prompt, yield one token. */
+PA_API int pa_sched_commit(pa_scheduler* s);
+
+/* Counters: waiting, running, finished requests and the tokens processed. */
+PA_API int pa_sched_stats(const pa_scheduler* s, int64_t* waiting, int64_t* running,
+                          int64_t* finished, int64_t* prefill_tokens, int64_t* decode_tokens);
+
+/*
+ * Device copy of whole blocks of the K and V pools: block dst[i] <- src[i]
+ * for i < n (src/dst are device int32 arrays). Used for copy-on-write.
+ */
+PA_API int pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src, const int32_t* dst, int n,
+                          int* d_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_SERVING_H */

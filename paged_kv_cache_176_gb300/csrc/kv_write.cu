@@ -6,6 +6,7 @@
 // row per token, done with 16-byte vector stores. The cache of a sequence
 // grows this way block by block ("Chunked Prefill" page, how chunked prefill
 // works; "vLLM serving internals", PagedAttention as a virtual memory system).
+#include "../../include/pa_serving.h"
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -39,6 +40,26 @@ __global__ void __launch_bounds__(128) kv_write_kernel(uint4* __restrict__ k_poo
   }
 }
 
+// One CTA per (src, dst) pair: copy block src of the K and V pools onto
+// block dst (copy-on-write of a shared block).
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_pool,
+                                                          uint4* __restrict__ v_pool,
+                                                          int64_t num_blocks, int vecs_per_block,
+                                                          const int32_t* __restrict__ src,
+                                                          const int32_t* __restrict__ dst,
+                                                          int* d_status) {
+  const int i = blockIdx.x;
+  const int64_t s = src[i], d = dst[i];
+  if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+    if (threadIdx.x == 0) status_or(d_status, PA_STATUS_BAD_BLOCK);
+    return;
+  }
+  for (int v = threadIdx.x; v < vecs_per_block; v += blockDim.x) {
+    k_pool[d * vecs_per_block + v] = k_pool[s * vecs_per_block + v];
+    v_pool[d * vecs_per_block + v] = v_pool[s * vecs_per_block + v];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream) {
@@ -55,3 +76,22 @@ cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace pa
+
+extern "C" int pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src, const int32_t* dst,
+                              int n, int* d_status, void* stream) {
+  if (pool == nullptr || pool->k == nullptr || pool->v == nullptr || n < 0) return PA_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(pool->k) & 15u) || (reinterpret_cast<uintptr_t>(pool->v) & 15u))
+    return PA_EINVAL;
+  if (pool->num_blocks <= 0 || pool->block_size != pa::kBlockSize) return PA_EUNSUPPORTED;
+  if (pool->dtype != PA_F32 && pool->dtype != PA_BF16) return PA_EUNSUPPORTED;
+  if (n == 0) return PA_OK;
+  if (src == nullptr || dst == nullptr) return PA_EINVAL;
+  const int64_t elt = pool->dtype == PA_BF16 ? 2 : 4;
+  const int64_t bytes = static_cast<int64_t>(pa::kBlockSize) * pool->num_kv_heads * pool->head_dim * elt;
+  if (bytes % 16 != 0) return PA_EUNSUPPORTED;
+  pa::copy_blocks_kernel<<<n, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(pool->k), static_cast<uint4*>(pool->v), pool->num_blocks,
+      static_cast<int>(bytes / 16), src, dst, d_status);
+  if (cudaGetLastError() != cudaSuccess) return PA_ECUDA;
+  return PA_OK;
+}

@@ -1,0 +1,321 @@
+// serving.cpp -- host-side block manager and iteration-level scheduler
+// (include/pa_serving.h). Plain C++17, no CUDA calls.
+#include <algorithm>
+#include <deque>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/pa_serving.h"
+
+struct pa_block_manager {
+  struct Seq {
+    std::vector<int32_t> blocks;
+    int64_t tokens = 0;
+  };
+  int64_t num_blocks = 0;
+  int block_size = 0;
+  std::vector<int32_t> free_list;  // a stack: the most recently freed block is reused first
+  std::vector<int32_t> refcount;
+  std::unordered_map<int64_t, Seq> seqs;
+
+  int64_t blocks_for(int64_t tokens) const { return (tokens + block_size - 1) / block_size; }
+
+  int32_t take() {
+    const int32_t b = free_list.back();
+    free_list.pop_back();
+    refcount[b] = 1;
+    return b;
+  }
+  void release(int32_t b) {
+    if (--refcount[b] == 0) free_list.push_back(b);
+  }
+  // Blocks an append of n tokens to s needs (a copy of a shared partial last
+  // block counts as one).
+  int64_t append_cost(const Seq& s, int n) const {
+    int64_t need = blocks_for(s.tokens + n) - blocks_for(s.tokens);
+    if (n > 0 && s.tokens % block_size != 0 && refcount[s.blocks.back()] > 1) need += 1;
+    return need;
+  }
+};
+
+extern "C" {
+
+pa_block_manager* pa_bm_create(int64_t num_blocks, int block_size) {
+  if (num_blocks <= 0 || num_blocks > INT32_MAX || block_size <= 0) return nullptr;
+  auto* bm = new (std::nothrow) pa_block_manager();
+  if (bm == nullptr) return nullptr;
+  bm->num_blocks = num_blocks;
+  bm->block_size = block_size;
+  bm->refcount.assign(static_cast<size_t>(num_blocks), 0);
+  bm->free_list.reserve(static_cast<size_t>(num_blocks));
+  // block 0 on top of the stack: allocation order 0, 1, 2, ...
+  for (int64_t b = num_blocks - 1; b >= 0; --b) bm->free_list.push_back(static_cast<int32_t>(b));
+  return bm;
+}
+
+void pa_bm_destroy(pa_block_manager* bm) { delete bm; }
+
+int64_t pa_bm_num_free(const pa_block_manager* bm) {
+  return bm ? static_cast<int64_t>(bm->free_list.size()) : -1;
+}
+
+int pa_bm_add(pa_block_manager* bm, int64_t seq) {
+  if (bm == nullptr || bm->seqs.count(seq)) return PA_EINVAL;
+  bm->seqs.emplace(seq, pa_block_manager::Seq());
+  return PA_OK;
+}
+
+int pa_bm_fork(pa_block_manager* bm, int64_t parent, int64_t child) {
+  if (bm == nullptr || !bm->seqs.count(parent) || bm->seqs.count(child)) return PA_EINVAL;
+  pa_block_manager::Seq copy = bm->seqs.at(parent);
+  for (int32_t b : copy.blocks) ++bm->refcount[b];
+  bm->seqs.emplace(child, std::move(copy));
+  return PA_OK;
+}
+
+int pa_bm_append(pa_block_manager* bm, int64_t seq, int n, int64_t* slots_out, int32_t* cow_src,
+                 int32_t* cow_dst, int* n_cow) {
+  if (bm == nullptr || n < 0 || (n > 0 && slots_out == nullptr)) return PA_EINVAL;
+  auto it = bm->seqs.find(seq);
+  if (it == bm->seqs.end()) return PA_EINVAL;
+  auto& s = it->second;
+  if (n_cow != nullptr) *n_cow = 0;
+  if (n == 0) return PA_OK;
+  if (bm->append_cost(s, n) > static_cast<int64_t>(bm->free_list.size())) return PA_ENOSPACE;
+  const int b = bm->block_size;
+  if (s.tokens % b != 0 && bm->refcount[s.blocks.back()] > 1) {
+    // the last block is shared and partially filled: give this sequence its
+    // own copy before writing into it
+    if (cow_src == nullptr || cow_dst == nullptr || n_cow == nullptr) return PA_EINVAL;
+    const int32_t old = s.blocks.back();
+    const int32_t fresh = bm->take();
+    bm->release(old);
+    s.blocks.back() = fresh;
+    cow_src[0] = old;
+    cow_dst[0] = fresh;
+    *n_cow = 1;
+  }
+  for (int i = 0; i < n; ++i) {
+    const int64_t pos = s.tokens + i;
+    if (pos % b == 0) s.blocks.push_back(bm->take());  // the sequence outgrew its blocks
+    slots_out[i] = static_cast<int64_t>(s.blocks[pos / b]) * b + pos % b;
+  }
+  s.tokens += n;
+  return PA_OK;
+}
+
+int pa_bm_free(pa_block_manager* bm, int64_t seq) {
+  if (bm == nullptr) return PA_EINVAL;
+  auto it = bm->seqs.find(seq);
+  if (it == bm->seqs.end()) return PA_EINVAL;
+  for (int32_t blk : it->second.blocks) bm->release(blk);
+  bm->seqs.erase(it);
+  return PA_OK;
+}
+
+int64_t pa_bm_num_tokens(const pa_block_manager* bm, int64_t seq) {
+  if (bm == nullptr) return -1;
+  auto it = bm->seqs.find(seq);
+  return it == bm->seqs.end() ? -1 : it->second.tokens;
+}
+
+int pa_bm_block_table(const pa_block_manager* bm, int64_t seq, int32_t* out, int max_blocks) {
+  if (bm == nullptr || out == nullptr || max_blocks < 0) return PA_EINVAL;
+  auto it = bm->seqs.find(seq);
+  if (it == bm->seqs.end()) return PA_EINVAL;
+  const auto& blocks = it->second.blocks;
+  if (static_cast<int64_t>(blocks.size()) > max_blocks) return PA_EINVAL;
+  std::copy(blocks.begin(), blocks.end(), out);
+  return static_cast<int>(blocks.size());
+}
+
+int pa_bm_refcount(const pa_block_manager* bm, int32_t block) {
+  if (bm == nullptr || block < 0 || block >= bm->num_blocks) return -1;
+  return bm->refcount[block];
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ scheduler
+
+struct pa_scheduler {
+  struct Req {
+    int64_t id;
+    int64_t prompt;
+    int64_t max_new;
+    int64_t prefilled = 0;
+    int64_t generated = 0;
+    int64_t reserve = 0;   // blocks the request may ever hold
+    int64_t step_n = 0;    // tokens scheduled in the pending step
+    bool step_prefill = false;
+  };
+  pa_block_manager* bm = nullptr;
+  int budget = 0, chunk = 0, max_running = 0;
+  std::deque<Req> waiting;
+  std::vector<Req> running;
+  std::unordered_map<int64_t, char> known;
+  int64_t finished = 0, prefill_tokens = 0, decode_tokens = 0;
+  bool pending = false;
+
+  int64_t held(const Req& r) const {
+    auto it = bm->seqs.find(r.id);
+    return it == bm->seqs.end() ? 0 : static_cast<int64_t>(it->second.blocks.size());
+  }
+  // free blocks not promised to running requests
+  int64_t spare() const {
+    int64_t promised = 0;
+    for (const Req& r : running) promised += std::max<int64_t>(0, r.reserve - held(r));
+    return static_cast<int64_t>(bm->free_list.size()) - promised;
+  }
+};
+
+extern "C" {
+
+pa_scheduler* pa_sched_create(pa_block_manager* bm, int token_budget, int chunk_size,
+                              int max_running) {
+  if (bm == nullptr || token_budget <= 0 || chunk_size <= 0 || max_running <= 0) return nullptr;
+  auto* s = new (std::nothrow) pa_scheduler();
+  if (s == nullptr) return nullptr;
+  s->bm = bm;
+  s->budget = token_budget;
+  s->chunk = chunk_size;
+  s->max_running = max_running;
+  return s;
+}
+
+void pa_sched_destroy(pa_scheduler* s) { delete s; }
+
+int pa_sched_submit(pa_scheduler* s, int64_t req_id, int prompt_len, int max_new_tokens) {
+  if (s == nullptr || prompt_len < 1 || max_new_tokens < 1 || s->known.count(req_id)) return PA_EINVAL;
+  pa_scheduler::Req r;
+  r.id = req_id;
+  r.prompt = prompt_len;
+  r.max_new = max_new_tokens;
+  r.reserve = s->bm->blocks_for(static_cast<int64_t>(prompt_len) + max_new_tokens);
+  if (r.reserve > s->bm->num_blocks) return PA_ENOSPACE;  // can never fit
+  s->known.emplace(req_id, 1);
+  s->waiting.push_back(r);
+  return PA_OK;
+}
+
+int pa_sched_step(pa_scheduler* s, pa_step_plan* plan) {
+  if (s == nullptr || plan == nullptr || s->pending) return PA_EINVAL;
+  pa_block_manager* bm = s->bm;
+  // 1. finished sequences leave and return their blocks
+  for (size_t i = 0; i < s->running.size();) {
+    if (s->running[i].generated >= s->running[i].max_new) {
+      pa_bm_free(bm, s->running[i].id);
+      ++s->finished;
+      s->running.erase(s->running.begin() + static_cast<long>(i));
+    } else {
+      ++i;
+    }
+  }
+  // 2. admit waiting requests (FIFO) while their blocks fit
+  while (!s->waiting.empty() && static_cast<int>(s->running.size()) < s->max_running &&
+         s->spare() >= s->waiting.front().reserve) {
+    pa_scheduler::Req r = s->waiting.front();
+    s->waiting.pop_front();
+    pa_bm_add(bm, r.id);
+    s->running.push_back(r);
+  }
+  // 3. one token per running decode, then prefill chunks, under the budget
+  std::vector<size_t> order;
+  int64_t tokens = 0;
+  for (size_t i = 0; i < s->running.size(); ++i) {
+    auto& r = s->running[i];
+    r.step_n = 0;
+    if (r.prefilled == r.prompt && r.generated < r.max_new && tokens + 1 <= s->budget) {
+      r.step_n = 1;
+      r.step_prefill = false;
+      tokens += 1;
+      order.push_back(i);
+    }
+  }
+  const size_t num_decode = order.size();
+  for (size_t i = 0; i < s->running.size(); ++i) {
+    auto& r = s->running[i];
+    if (r.prefilled >= r.prompt) continue;
+    const int64_t n = std::min<int64_t>({static_cast<int64_t>(s->chunk), r.prompt - r.prefilled,
+                                         s->budget - tokens});
+    if (n <= 0) break;
+    r.step_n = n;
+    r.step_prefill = true;
+    tokens += n;
+    order.push_back(i);
+  }
+  // capacities
+  int64_t max_blocks = 0;
+  for (size_t k : order) {
+    const auto& r = s->running[k];
+    const auto it = bm->seqs.find(r.id);
+    max_blocks = std::max(max_blocks, bm->blocks_for(it->second.tokens + r.step_n));
+  }
+  if (static_cast<int64_t>(order.size()) > plan->max_seqs || tokens > plan->max_tokens ||
+      max_blocks > plan->max_blocks_per_seq) {
+    for (auto& r : s->running) r.step_n = 0;
+    return PA_EINVAL;
+  }
+  // 4. reserve slots and fill the plan
+  plan->num_seqs = static_cast<int>(order.size());
+  plan->num_tokens = static_cast<int>(tokens);
+  plan->num_decode = static_cast<int>(num_decode);
+  plan->num_cow = 0;
+  plan->cu_q_lens[0] = 0;
+  int64_t t = 0;
+  for (size_t j = 0; j < order.size(); ++j) {
+    const auto& r = s->running[order[j]];
+    int32_t src = -1, dst = -1;
+    int n_cow = 0;
+    const int rc = pa_bm_append(bm, r.id, static_cast<int>(r.step_n), plan->slot_mapping + t, &src,
+                                &dst, &n_cow);
+    if (rc != PA_OK) return rc;  // cannot happen: admission reserved the blocks
+    if (n_cow > 0) {
+      if (plan->num_cow >= plan->max_cow) return PA_EINVAL;
+      plan->cow_src[plan->num_cow] = src;
+      plan->cow_dst[plan->num_cow] = dst;
+      ++plan->num_cow;
+    }
+    t += r.step_n;
+    plan->seq_ids[j] = r.id;
+    plan->cu_q_lens[j + 1] = static_cast<int32_t>(t);
+    plan->context_lens[j] = static_cast<int32_t>(bm->seqs.at(r.id).tokens);
+    int32_t* row = plan->block_tables + j * static_cast<int64_t>(plan->max_blocks_per_seq);
+    const int nb = pa_bm_block_table(bm, r.id, row, plan->max_blocks_per_seq);
+    for (int k = nb; k < plan->max_blocks_per_seq; ++k) row[k] = -1;
+  }
+  s->pending = plan->num_seqs > 0;
+  return PA_OK;
+}
+
+int pa_sched_commit(pa_scheduler* s) {
+  if (s == nullptr || !s->pending) return PA_EINVAL;
+  for (auto& r : s->running) {
+    if (r.step_n == 0) continue;
+    if (r.step_prefill) {
+      r.prefilled += r.step_n;
+      s->prefill_tokens += r.step_n;
+      if (r.prefilled == r.prompt) r.generated += 1;  // the last chunk yields the first token
+    } else {
+      r.generated += 1;
+      s->decode_tokens += 1;
+    }
+    r.step_n = 0;
+  }
+  s->pending = false;
+  return PA_OK;
+}
+
+int pa_sched_stats(const pa_scheduler* s, int64_t* waiting, int64_t* running, int64_t* finished,
+                   int64_t* prefill_tokens, int64_t* decode_tokens) {
+  if (s == nullptr) return PA_EINVAL;
+  if (waiting) *waiting = static_cast<int64_t>(s->waiting.size());
+  if (running) *running = static_cast<int64_t>(s->running.size());
+  if (finished) *finished = s->finished;
+  if (prefill_tokens) *prefill_tokens = s->prefill_tokens;
+  if (decode_tokens) *decode_tokens = s->decode_tokens;
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,289 @@
+"""Block manager, scheduler and a serving loop over libpa (include/pa_serving.h).
+
+``BlockManager`` and ``Scheduler`` are ctypes bindings of the native C++
+objects (argument marshalling only). ``ServingLoop`` drives them: every step
+it asks the scheduler for a batch (decode tokens first, then prefill chunks
+under the token budget), copies the plan to the device, runs the
+copy-on-write block copies and one ``pa_mixed_step`` (the step's KV write
+fused in) over the paged pool, then commits the step. There is no model: the
+new tokens' q/k/v are seeded random values, which is all the attention path
+needs.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import abi
+
+PA_ENOSPACE = -6
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [
+        ("max_seqs", ctypes.c_int), ("max_tokens", ctypes.c_int),
+        ("max_blocks_per_seq", ctypes.c_int), ("max_cow", ctypes.c_int),
+        ("num_seqs", ctypes.c_int), ("num_tokens", ctypes.c_int),
+        ("num_decode", ctypes.c_int), ("num_cow", ctypes.c_int),
+        ("seq_ids", ctypes.c_void_p), ("cu_q_lens", ctypes.c_void_p),
+        ("context_lens", ctypes.c_void_p), ("block_tables", ctypes.c_void_p),
+        ("slot_mapping", ctypes.c_void_p), ("cow_src", ctypes.c_void_p),
+        ("cow_dst", ctypes.c_void_p),
+    ]
+
+
+_ready = False
+
+
+def _lib() -> ctypes.CDLL:
+    global _ready
+    lib = abi.load()
+    if not _ready:
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        lib.pa_bm_create.restype = P
+        lib.pa_bm_create.argtypes = [I64, I]
+        lib.pa_bm_destroy.restype = None
+        lib.pa_bm_destroy.argtypes = [P]
+        lib.pa_bm_num_free.restype = I64
+        lib.pa_bm_num_free.argtypes = [P]
+        lib.pa_bm_add.restype = I
+        lib.pa_bm_add.argtypes = [P, I64]
+        lib.pa_bm_fork.restype = I
+        lib.pa_bm_fork.argtypes = [P, I64, I64]
+        lib.pa_bm_append.restype = I
+        lib.pa_bm_append.argtypes = [P, I64, I, P, P, P, P]
+        lib.pa_bm_free.restype = I
+        lib.pa_bm_free.argtypes = [P, I64]
+        lib.pa_bm_num_tokens.restype = I64
+        lib.pa_bm_num_tokens.argtypes = [P, I64]
+        lib.pa_bm_block_table.restype = I
+        lib.pa_bm_block_table.argtypes = [P, I64, P, I]
+        lib.pa_bm_refcount.restype = I
+        lib.pa_bm_refcount.argtypes = [P, ctypes.c_int32]
+        lib.pa_sched_create.restype = P
+        lib.pa_sched_create.argtypes = [P, I, I, I]
+        lib.pa_sched_destroy.restype = None
+        lib.pa_sched_destroy.argtypes = [P]
+        lib.pa_sched_submit.restype = I
+        lib.pa_sched_submit.argtypes = [P, I64, I, I]
+        lib.pa_sched_step.restype = I
+        lib.pa_sched_step.argtypes = [P, ctypes.POINTER(_Plan)]
+        lib.pa_sched_commit.restype = I
+        lib.pa_sched_commit.argtypes = [P]
+        lib.pa_sched_stats.restype = I
+        lib.pa_sched_stats.argtypes = [P, P, P, P, P, P]
+        lib.pa_copy_blocks.restype = I
+        lib.pa_copy_blocks.argtypes = [ctypes.POINTER(abi.pa_kv_pool), P, P, I, P, P]
+        _ready = True
+    return lib
+
+
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class BlockManager:
+    """Pool of ``num_blocks`` blocks of ``block_size`` tokens (native)."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        self._lib = _lib()
+        self.block_size = block_size
+        self.num_blocks = num_blocks
+        self._h = self._lib.pa_bm_create(num_blocks, block_size)
+        if not self._h:
+            raise ValueError("bad block manager sizes")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.pa_bm_destroy(h)
+            self._h = None
+
+    @property
+    def num_free(self) -> int:
+        return int(self._lib.pa_bm_num_free(self._h))
+
+    def add(self, seq: int) -> None:
+        abi._check("pa_bm_add", self._lib.pa_bm_add(self._h, seq))
+
+    def fork(self, parent: int, child: int) -> None:
+        abi._check("pa_bm_fork", self._lib.pa_bm_fork(self._h, parent, child))
+
+    def append(self, seq: int, n: int):
+        """Slots of n new tokens and the copy-on-write pairs [(src, dst)]."""
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        src = np.empty(1, dtype=np.int32)
+        dst = np.empty(1, dtype=np.int32)
+        n_cow = ctypes.c_int(0)
+        rc = self._lib.pa_bm_append(self._h, seq, n, _np_ptr(slots), _np_ptr(src), _np_ptr(dst),
+                                    ctypes.byref(n_cow))
+        abi._check("pa_bm_append", rc)
+        cow = [(int(src[0]), int(dst[0]))] if n_cow.value else []
+        return slots[:n], cow
+
+    def free(self, seq: int) -> None:
+        abi._check("pa_bm_free", self._lib.pa_bm_free(self._h, seq))
+
+    def num_tokens(self, seq: int) -> int:
+        return int(self._lib.pa_bm_num_tokens(self._h, seq))
+
+    def block_table(self, seq: int, max_blocks: int = 1 << 16) -> np.ndarray:
+        out = np.empty(max_blocks, dtype=np.int32)
+        n = self._lib.pa_bm_block_table(self._h, seq, _np_ptr(out), max_blocks)
+        if n < 0:
+            raise abi.PagedAttentionError("pa_bm_block_table", n)
+        return out[:n].copy()
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.pa_bm_refcount(self._h, block))
+
+
+class StepPlan:
+    """Host buffers of one scheduler step (see pa_step_plan)."""
+
+    def __init__(self, max_seqs: int, max_tokens: int, max_blocks_per_seq: int, max_cow: int = 64):
+        self.seq_ids = np.zeros(max_seqs, dtype=np.int64)
+        self.cu_q_lens = np.zeros(max_seqs + 1, dtype=np.int32)
+        self.context_lens = np.zeros(max_seqs, dtype=np.int32)
+        self.block_tables = np.full((max_seqs, max_blocks_per_seq), -1, dtype=np.int32)
+        self.slot_mapping = np.zeros(max_tokens, dtype=np.int64)
+        self.cow_src = np.zeros(max_cow, dtype=np.int32)
+        self.cow_dst = np.zeros(max_cow, dtype=np.int32)
+        self.c = _Plan(max_seqs, max_tokens, max_blocks_per_seq, max_cow, 0, 0, 0, 0,
+                       _np_ptr(self.seq_ids).value, _np_ptr(self.cu_q_lens).value,
+                       _np_ptr(self.context_lens).value, _np_ptr(self.block_tables).value,
+                       _np_ptr(self.slot_mapping).value, _np_ptr(self.cow_src).value,
+                       _np_ptr(self.cow_dst).value)
+
+    @property
+    def num_seqs(self) -> int:
+        return self.c.num_seqs
+
+    @property
+    def num_tokens(self) -> int:
+        return self.c.num_tokens
+
+    @property
+    def num_decode(self) -> int:
+        return self.c.num_decode
+
+    @property
+    def num_cow(self) -> int:
+        return self.c.num_cow
+
+
+class Scheduler:
+    """Iteration-level scheduler with chunked prefill (native)."""
+
+    def __init__(self, bm: BlockManager, token_budget: int, chunk_size: int, max_running: int):
+        self._lib = _lib()
+        self.bm = bm  # keep the block manager alive
+        self.token_budget = token_budget
+        self._h = self._lib.pa_sched_create(bm._h, token_budget, chunk_size, max_running)
+        if not self._h:
+            raise ValueError("bad scheduler arguments")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.pa_sched_destroy(h)
+            self._h = None
+
+    def submit(self, req_id: int, prompt_len: int, max_new_tokens: int) -> None:
+        abi._check("pa_sched_submit", self._lib.pa_sched_submit(self._h, req_id, prompt_len,
+                                                                  max_new_tokens))
+
+    def step(self, plan: StepPlan) -> StepPlan:
+        abi._check("pa_sched_step", self._lib.pa_sched_step(self._h, ctypes.byref(plan.c)))
+        return plan
+
+    def commit(self) -> None:
+        abi._check("pa_sched_commit", self._lib.pa_sched_commit(self._h))
+
+    def stats(self) -> dict:
+        v = [ctypes.c_int64(0) for _ in range(5)]
+        abi._check("pa_sched_stats", self._lib.pa_sched_stats(self._h, *[ctypes.byref(x) for x in v]))
+        keys = ("waiting", "running", "finished", "prefill_tokens", "decode_tokens")
+        return {k: int(x.value) for k, x in zip(keys, v)}
+
+
+def pa_copy_blocks(k_pool, v_pool, src: torch.Tensor, dst: torch.Tensor, d_status=None,
+                   stream=None) -> None:
+    """Device copy of whole K/V blocks src[i] -> dst[i] (copy-on-write)."""
+    lib = _lib()
+    pool = abi.make_pool(k_pool, v_pool)
+    n = int(src.numel())
+    abi._check("pa_copy_blocks", lib.pa_copy_blocks(ctypes.byref(pool), abi._ptr(src),
+                                                    abi._ptr(dst), n, abi._ptr(d_status),
+                                                    abi._stream(stream)))
+
+
+class ServingLoop:
+    """Continuous batching with chunked prefill over one layer's paged pool."""
+
+    def __init__(self, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 dtype=torch.bfloat16, token_budget: int = 2048, chunk_size: int = 512,
+                 max_running: int = 256, max_context: int = 32768, device="cuda", seed: int = 0,
+                 stream: Optional[torch.cuda.Stream] = None):
+        self.bm = BlockManager(num_blocks, 16)
+        self.sched = Scheduler(self.bm, token_budget, chunk_size, max_running)
+        self.hq, self.hkv, self.d, self.dtype = num_q_heads, num_kv_heads, head_dim, dtype
+        self.budget = token_budget
+        self.device = torch.device(device)
+        self.stream = stream or torch.cuda.current_stream(self.device)
+        mb = (max_context + 15) // 16
+        self.max_blocks = mb
+        self.plan = StepPlan(max_running, token_budget, mb)
+        self.k_pool = torch.full((num_blocks, 16, num_kv_heads, head_dim), float("nan"), dtype=dtype,
+                                 device=self.device)
+        self.v_pool = torch.full_like(self.k_pool, float("nan"))
+        T, S = token_budget, max_running
+        self.q = torch.empty(T, num_q_heads, head_dim, dtype=dtype, device=self.device)
+        self.k_new = torch.empty(T, num_kv_heads, head_dim, dtype=dtype, device=self.device)
+        self.v_new = torch.empty_like(self.k_new)
+        self.out = torch.empty_like(self.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.d_cu = torch.empty(S + 1, dtype=torch.int32, device=self.device)
+        self.d_ctx = torch.empty(S, dtype=torch.int32, device=self.device)
+        self.d_bt = torch.empty(S, mb, dtype=torch.int32, device=self.device)
+        self.d_slots = torch.empty(T, dtype=torch.int64, device=self.device)
+        self.d_cow = torch.empty(2, 64, dtype=torch.int32, device=self.device)
+        self.ws = torch.empty(abi.pa_mixed_workspace_size(S, T, num_q_heads, head_dim, mb),
+                              dtype=torch.uint8, device=self.device)
+        self.gen = torch.Generator(device=self.device)
+        self.gen.manual_seed(seed)
+        self.scale = head_dim ** -0.5
+        self.steps = 0
+
+    def submit(self, req_id: int, prompt_len: int, max_new_tokens: int) -> None:
+        self.sched.submit(req_id, prompt_len, max_new_tokens)
+
+    def step(self) -> Optional[StepPlan]:
+        """Run one step; returns its plan (host arrays), or None when idle."""
+        p = self.sched.step(self.plan)
+        S, T = p.num_seqs, p.num_tokens
+        if S == 0:
+            return None
+        with torch.cuda.stream(self.stream):
+            for t in (self.q[:T], self.k_new[:T], self.v_new[:T]):
+                t.copy_(torch.randn(t.shape, generator=self.gen, device=self.device, dtype=torch.float32))
+            self.d_cu[:S + 1].copy_(torch.from_numpy(p.cu_q_lens[:S + 1]), non_blocking=False)
+            self.d_ctx[:S].copy_(torch.from_numpy(p.context_lens[:S]))
+            self.d_bt[:S].copy_(torch.from_numpy(p.block_tables[:S]))
+            self.d_slots[:T].copy_(torch.from_numpy(p.slot_mapping[:T]))
+            if p.num_cow:
+                self.d_cow[0, :p.num_cow].copy_(torch.from_numpy(p.cow_src[:p.num_cow]))
+                self.d_cow[1, :p.num_cow].copy_(torch.from_numpy(p.cow_dst[:p.num_cow]))
+                pa_copy_blocks(self.k_pool, self.v_pool, self.d_cow[0, :p.num_cow],
+                               self.d_cow[1, :p.num_cow], d_status=self.status, stream=self.stream)
+            abi.pa_mixed_step(self.out[:T], self.q[:T], self.d_cu[:S + 1], self.d_ctx[:S],
+                              self.d_bt[:S], self.k_pool, self.v_pool, self.scale, self.budget,
+                              k_new=self.k_new[:T], v_new=self.v_new[:T],
+                              slot_mapping=self.d_slots[:T], workspace=self.ws,
+                              d_status=self.status, stream=self.stream)
+        self.sched.commit()
+        self.steps += 1
+        return p
