@@ -29,6 +29,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -273,6 +275,10 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                                 W.shared_prefix_decode(seed=args.seed), dev, stream),
         ]
 
+    serving = None
+    if not args.skip_serving:
+        serving = run_serving(args, dev, stream)
+
     pk = peaks()
     decode_gbs = nb["decode"] / (decode_ms * 1e-3) / 1e9
     src = os.path.join(ROOT, "paged_kv_cache_176_gb300", "csrc", "decode_impl.cuh")
@@ -314,6 +320,8 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         res["mixed_step"] = mixed
     if extra is not None:
         res["other_decode_workloads"] = extra
+    if serving is not None:
+        res["serving_loop"] = serving
     return res
 
 
@@ -424,6 +432,96 @@ def run_mixed(args, dev, stream) -> dict:
         "decode_gbs_step": round(work["decode_bytes"] / (ms * 1e-3) / 1e9, 1),
         "prefill_flops": work["prefill_flops"],
         "decode_bytes": work["decode_bytes"],
+    }
+
+
+SERVING_WORKLOAD = ("serving_stream_bf16: 1024 requests, prompt U[512,4096], new tokens "
+                    "U[22,356]; budget 2048, chunk 512, <= 256 running; 64/8 heads, d 128; "
+                    "pool 65536 blocks")
+
+
+def serving_requests(seed: int, n: int, prompt=(512, 4096), new=(22, 356)):
+    g = np.random.default_rng(seed + 7)
+    return [(int(g.integers(prompt[0], prompt[1] + 1)), int(g.integers(new[0], new[1] + 1)))
+            for _ in range(n)]
+
+
+def run_serving(args, dev, stream) -> dict:
+    """Continuous batching through the native scheduler and pa_mixed_step:
+    the whole loop (host planning, one pinned plan copy per step, CoW block
+    copies, the fused KV write and the attention) from the first request to
+    the last token. Throughput counts query tokens (prefill + decode)."""
+    import torch
+    from paged_kv_cache_176_gb300.serving import ServingLoop
+
+    def make():
+        return ServingLoop(65536, 64, 8, 128, dtype=torch.bfloat16, token_budget=2048,
+                           chunk_size=512, max_running=256, max_context=4096 + 512, device=dev,
+                           seed=args.seed, stream=stream, fresh_inputs=False)
+
+    # warm-up stream, every step checked: packed tables and the paging bound
+    loop = make()
+    for rid, (pl, nn) in enumerate(serving_requests(args.seed + 1, 48)):
+        loop.submit(rid, pl, nn)
+    waste_max = 0
+    while True:
+        p = loop.step()
+        if p is None:
+            break
+        S = p.num_seqs
+        held = (p.tables >= 0).sum(axis=1)
+        ctx = p.context_lens[:S].astype(np.int64)
+        assert np.all(held == (ctx + 15) // 16)
+        waste_max = max(waste_max, int((held * 16 - ctx).max()))
+    torch.cuda.synchronize(dev)
+    assert int(loop.status.item()) == 0 and loop.bm.num_free == 65536
+    del loop
+
+    reqs = serving_requests(args.seed, 1024)
+    loop = make()
+    for rid, (pl, nn) in enumerate(reqs):
+        loop.submit(rid, pl, nn)
+    torch.cuda.synchronize(dev)
+    evs, toks, used = [], [], []
+    e0 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    t0 = time.perf_counter()
+    while True:
+        p = loop.step()
+        if p is None:
+            break
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(stream)
+        evs.append(ev)
+        toks.append(p.num_tokens)
+        used.append(loop.bm.num_blocks - loop.bm.num_free)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    assert int(loop.status.item()) == 0
+    st = loop.sched.stats()
+    assert st["finished"] == len(reqs)
+    dev_s = e0.elapsed_time(evs[-1]) * 1e-3
+    total = sum(toks)
+    # steady state: from the first to the last step that filled the budget
+    full = [i for i, t in enumerate(toks) if t == 2048]
+    i0, i1 = full[0], full[-1]
+    steady_s = evs[i0].elapsed_time(evs[i1]) * 1e-3 if i1 > i0 else float("nan")
+    steady_tok = sum(toks[i0 + 1:i1 + 1])
+    return {
+        "workload": SERVING_WORKLOAD,
+        "steps": len(toks),
+        "wall_s": round(wall, 4),
+        "tokens_per_s": round(total / wall, 1),
+        "device_tokens_per_s": round(total / dev_s, 1),
+        "steady_tokens_per_s": round(steady_tok / steady_s, 1),
+        "steady_steps": i1 - i0,
+        "prefill_tokens": st["prefill_tokens"],
+        "decode_tokens": st["decode_tokens"],
+        "decode_tokens_per_s": round(st["decode_tokens"] / wall, 1),
+        "mean_tokens_per_step": round(total / len(toks), 1),
+        "peak_blocks_in_use": max(used),
+        "h2d_plan_bytes_per_step": round(loop.h2d_bytes / len(toks), 1),
+        "max_waste_tokens_per_seq": waste_max,
     }
 
 
@@ -543,6 +641,10 @@ def main() -> None:
     ap.add_argument("--only-mixed", action="store_true",
                     help="run only the mixed step (profiling); prints its measurement")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-serving", action="store_true",
+                    help="skip the continuous-batching serving-loop measurement")
+    ap.add_argument("--only-serving", action="store_true",
+                    help="run only the serving-loop measurement (1 GPU)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=8.0)
     args = ap.parse_args()
@@ -558,11 +660,12 @@ def main() -> None:
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group(backend)
-    if args.only_mixed and args.impl != "reference":
+    if (args.only_mixed or args.only_serving) and args.impl != "reference":
         import torch
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
         torch.cuda.set_device(dev)
-        res = run_mixed(args, dev, torch.cuda.Stream(dev))
+        run = run_mixed if args.only_mixed else run_serving
+        res = run(args, dev, torch.cuda.Stream(dev))
     elif args.impl == "reference":
         res = run_reference(args, rank, world)
     else:

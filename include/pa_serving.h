@@ -90,14 +90,18 @@ PA_API void pa_sched_destroy(pa_scheduler* s);
 PA_API int pa_sched_submit(pa_scheduler* s, int64_t req_id, int prompt_len, int max_new_tokens);
 
 /* One step's batch, in caller-owned host buffers of the stated capacities.
- * Sequences are ordered decode first (q_len 1), then prefill chunks. */
+ * Sequences are ordered decode first (q_len 1), then prefill chunks. The
+ * block tables are packed: row j starts at j * table_stride, where
+ * table_stride (<= max_blocks_per_seq) is the largest block count of any
+ * sequence in the step, and is padded with -1 up to table_stride. */
 typedef struct {
   int max_seqs, max_tokens, max_blocks_per_seq, max_cow; /* capacities (in) */
   int num_seqs, num_tokens, num_decode, num_cow;         /* counts (out) */
+  int table_stride;                                      /* (out) */
   int64_t* seq_ids;       /* [max_seqs] */
   int32_t* cu_q_lens;     /* [max_seqs + 1] */
   int32_t* context_lens;  /* [max_seqs], including this step's tokens */
-  int32_t* block_tables;  /* [max_seqs * max_blocks_per_seq], -1 padded */
+  int32_t* block_tables;  /* [num_seqs * table_stride] used of max_seqs * max_blocks_per_seq */
   int64_t* slot_mapping;  /* [max_tokens] */
   int32_t* cow_src;       /* [max_cow] blocks to copy before the KV write */
   int32_t* cow_dst;       /* [max_cow] */

@@ -262,6 +262,7 @@ int pa_sched_step(pa_scheduler* s, pa_step_plan* plan) {
   plan->num_tokens = static_cast<int>(tokens);
   plan->num_decode = static_cast<int>(num_decode);
   plan->num_cow = 0;
+  plan->table_stride = static_cast<int>(std::max<int64_t>(max_blocks, 1));
   plan->cu_q_lens[0] = 0;
   int64_t t = 0;
   for (size_t j = 0; j < order.size(); ++j) {
@@ -281,9 +282,9 @@ int pa_sched_step(pa_scheduler* s, pa_step_plan* plan) {
     plan->seq_ids[j] = r.id;
     plan->cu_q_lens[j + 1] = static_cast<int32_t>(t);
     plan->context_lens[j] = static_cast<int32_t>(bm->seqs.at(r.id).tokens);
-    int32_t* row = plan->block_tables + j * static_cast<int64_t>(plan->max_blocks_per_seq);
-    const int nb = pa_bm_block_table(bm, r.id, row, plan->max_blocks_per_seq);
-    for (int k = nb; k < plan->max_blocks_per_seq; ++k) row[k] = -1;
+    int32_t* row = plan->block_tables + j * static_cast<int64_t>(plan->table_stride);
+    const int nb = pa_bm_block_table(bm, r.id, row, plan->table_stride);
+    for (int k = nb; k < plan->table_stride; ++k) row[k] = -1;
   }
   s->pending = plan->num_seqs > 0;
   return PA_OK;

@@ -28,6 +28,7 @@ class _Plan(ctypes.Structure):
         ("max_blocks_per_seq", ctypes.c_int), ("max_cow", ctypes.c_int),
         ("num_seqs", ctypes.c_int), ("num_tokens", ctypes.c_int),
         ("num_decode", ctypes.c_int), ("num_cow", ctypes.c_int),
+        ("table_stride", ctypes.c_int),
         ("seq_ids", ctypes.c_void_p), ("cu_q_lens", ctypes.c_void_p),
         ("context_lens", ctypes.c_void_p), ("block_tables", ctypes.c_void_p),
         ("slot_mapping", ctypes.c_void_p), ("cow_src", ctypes.c_void_p),
@@ -148,11 +149,11 @@ class StepPlan:
         self.seq_ids = np.zeros(max_seqs, dtype=np.int64)
         self.cu_q_lens = np.zeros(max_seqs + 1, dtype=np.int32)
         self.context_lens = np.zeros(max_seqs, dtype=np.int32)
-        self.block_tables = np.full((max_seqs, max_blocks_per_seq), -1, dtype=np.int32)
+        self.block_tables = np.full(max_seqs * max_blocks_per_seq, -1, dtype=np.int32)
         self.slot_mapping = np.zeros(max_tokens, dtype=np.int64)
         self.cow_src = np.zeros(max_cow, dtype=np.int32)
         self.cow_dst = np.zeros(max_cow, dtype=np.int32)
-        self.c = _Plan(max_seqs, max_tokens, max_blocks_per_seq, max_cow, 0, 0, 0, 0,
+        self.c = _Plan(max_seqs, max_tokens, max_blocks_per_seq, max_cow, 0, 0, 0, 0, 0,
                        _np_ptr(self.seq_ids).value, _np_ptr(self.cu_q_lens).value,
                        _np_ptr(self.context_lens).value, _np_ptr(self.block_tables).value,
                        _np_ptr(self.slot_mapping).value, _np_ptr(self.cow_src).value,
@@ -173,6 +174,16 @@ class StepPlan:
     @property
     def num_cow(self) -> int:
         return self.c.num_cow
+
+    @property
+    def table_stride(self) -> int:
+        return self.c.table_stride
+
+    @property
+    def tables(self) -> np.ndarray:
+        """This step's block tables, [num_seqs, table_stride] (-1 padded)."""
+        S, W = self.num_seqs, self.table_stride
+        return self.block_tables[:S * W].reshape(S, W)
 
 
 class Scheduler:
@@ -221,69 +232,127 @@ def pa_copy_blocks(k_pool, v_pool, src: torch.Tensor, dst: torch.Tensor, d_statu
                                                     abi._stream(stream)))
 
 
+def _align16(n: int) -> int:
+    return (n + 15) & ~15
+
+
 class ServingLoop:
-    """Continuous batching with chunked prefill over one layer's paged pool."""
+    """Continuous batching with chunked prefill over one layer's paged pool.
+
+    Each step's plan (slot mapping, cu_q_lens, context lengths, copy-on-write
+    pairs and the packed block tables) is packed into one of two pinned host
+    buffers and sent with a single asynchronous copy on ``stream``; the host
+    then plans the next step while the device runs this one. A pinned buffer
+    is refilled only after the copy that read it has finished.
+
+    With ``fresh_inputs`` the step's q/k/v are redrawn on the device every
+    step; otherwise the buffers keep the values drawn at construction (the
+    kernels' work does not depend on the values).
+    """
 
     def __init__(self, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                  dtype=torch.bfloat16, token_budget: int = 2048, chunk_size: int = 512,
                  max_running: int = 256, max_context: int = 32768, device="cuda", seed: int = 0,
-                 stream: Optional[torch.cuda.Stream] = None):
+                 stream: Optional[torch.cuda.Stream] = None, fresh_inputs: bool = True,
+                 max_cow: int = 64):
         self.bm = BlockManager(num_blocks, 16)
         self.sched = Scheduler(self.bm, token_budget, chunk_size, max_running)
         self.hq, self.hkv, self.d, self.dtype = num_q_heads, num_kv_heads, head_dim, dtype
         self.budget = token_budget
         self.device = torch.device(device)
         self.stream = stream or torch.cuda.current_stream(self.device)
+        self.fresh_inputs = fresh_inputs
         mb = (max_context + 15) // 16
         self.max_blocks = mb
-        self.plan = StepPlan(max_running, token_budget, mb)
+        T, S = token_budget, max_running
+        self.plan = StepPlan(S, T, mb, max_cow)
         self.k_pool = torch.full((num_blocks, 16, num_kv_heads, head_dim), float("nan"), dtype=dtype,
                                  device=self.device)
         self.v_pool = torch.full_like(self.k_pool, float("nan"))
-        T, S = token_budget, max_running
         self.q = torch.empty(T, num_q_heads, head_dim, dtype=dtype, device=self.device)
         self.k_new = torch.empty(T, num_kv_heads, head_dim, dtype=dtype, device=self.device)
         self.v_new = torch.empty_like(self.k_new)
         self.out = torch.empty_like(self.q)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
-        self.d_cu = torch.empty(S + 1, dtype=torch.int32, device=self.device)
-        self.d_ctx = torch.empty(S, dtype=torch.int32, device=self.device)
-        self.d_bt = torch.empty(S, mb, dtype=torch.int32, device=self.device)
-        self.d_slots = torch.empty(T, dtype=torch.int64, device=self.device)
-        self.d_cow = torch.empty(2, 64, dtype=torch.int32, device=self.device)
+        # packed plan: slots (int64) | cu (S+1) | ctx (S) | cow src | cow dst | tables
+        self._cap = (_align16(8 * T) + _align16(4 * (S + 1)) + _align16(4 * S) +
+                     2 * _align16(4 * max_cow) + _align16(4 * S * mb))
+        self._dev = torch.empty(self._cap, dtype=torch.uint8, device=self.device)
+        self._host = [torch.empty(self._cap, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+        self._host_np = [h.numpy() for h in self._host]
+        self._sent = [None, None]
+        self._k = 0
+        self.h2d_bytes = 0
         self.ws = torch.empty(abi.pa_mixed_workspace_size(S, T, num_q_heads, head_dim, mb),
                               dtype=torch.uint8, device=self.device)
         self.gen = torch.Generator(device=self.device)
         self.gen.manual_seed(seed)
+        with torch.cuda.stream(self.stream):
+            self._draw(T)
         self.scale = head_dim ** -0.5
         self.steps = 0
+
+    def _draw(self, T: int) -> None:
+        for t in (self.q[:T], self.k_new[:T], self.v_new[:T]):
+            t.copy_(torch.randn(t.shape, generator=self.gen, device=self.device, dtype=torch.float32))
 
     def submit(self, req_id: int, prompt_len: int, max_new_tokens: int) -> None:
         self.sched.submit(req_id, prompt_len, max_new_tokens)
 
+    def _pack(self, p: StepPlan):
+        """Pack the plan into the free pinned buffer; returns the byte offsets."""
+        S, T, C, W = p.num_seqs, p.num_tokens, p.num_cow, p.table_stride
+        k = self._k
+        if self._sent[k] is not None:
+            self._sent[k].synchronize()  # the copy that read this buffer is done
+        buf = self._host_np[k]
+        offs = {}
+        o = 0
+        for name, src, dt in (("slots", p.slot_mapping[:T], np.int64),
+                              ("cu", p.cu_q_lens[:S + 1], np.int32),
+                              ("ctx", p.context_lens[:S], np.int32),
+                              ("src", p.cow_src[:C], np.int32),
+                              ("dst", p.cow_dst[:C], np.int32),
+                              ("bt", p.block_tables[:S * W], np.int32)):
+            n = src.size * np.dtype(dt).itemsize
+            buf[o:o + n].view(dt)[:] = src
+            offs[name] = (o, src.size)
+            o = _align16(o + n)
+        return k, o, offs
+
+    def _view(self, offs, name, dtype):
+        o, n = offs[name]
+        size = torch.tensor([], dtype=dtype).element_size()
+        return self._dev[o:o + n * size].view(dtype)
+
     def step(self) -> Optional[StepPlan]:
-        """Run one step; returns its plan (host arrays), or None when idle."""
+        """Enqueue one step on ``stream``; returns its plan (host arrays), or
+        None when every request has finished. The host does not wait for the
+        device, except to reuse a pinned buffer."""
         p = self.sched.step(self.plan)
-        S, T = p.num_seqs, p.num_tokens
+        S, T, C = p.num_seqs, p.num_tokens, p.num_cow
         if S == 0:
             return None
+        k, nbytes, offs = self._pack(p)
         with torch.cuda.stream(self.stream):
-            for t in (self.q[:T], self.k_new[:T], self.v_new[:T]):
-                t.copy_(torch.randn(t.shape, generator=self.gen, device=self.device, dtype=torch.float32))
-            self.d_cu[:S + 1].copy_(torch.from_numpy(p.cu_q_lens[:S + 1]), non_blocking=False)
-            self.d_ctx[:S].copy_(torch.from_numpy(p.context_lens[:S]))
-            self.d_bt[:S].copy_(torch.from_numpy(p.block_tables[:S]))
-            self.d_slots[:T].copy_(torch.from_numpy(p.slot_mapping[:T]))
-            if p.num_cow:
-                self.d_cow[0, :p.num_cow].copy_(torch.from_numpy(p.cow_src[:p.num_cow]))
-                self.d_cow[1, :p.num_cow].copy_(torch.from_numpy(p.cow_dst[:p.num_cow]))
-                pa_copy_blocks(self.k_pool, self.v_pool, self.d_cow[0, :p.num_cow],
-                               self.d_cow[1, :p.num_cow], d_status=self.status, stream=self.stream)
-            abi.pa_mixed_step(self.out[:T], self.q[:T], self.d_cu[:S + 1], self.d_ctx[:S],
-                              self.d_bt[:S], self.k_pool, self.v_pool, self.scale, self.budget,
-                              k_new=self.k_new[:T], v_new=self.v_new[:T],
-                              slot_mapping=self.d_slots[:T], workspace=self.ws,
-                              d_status=self.status, stream=self.stream)
+            if self.fresh_inputs:
+                self._draw(T)
+            self._dev[:nbytes].copy_(self._host[k][:nbytes], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(self.stream)
+            self._sent[k] = ev
+            self._k ^= 1
+            self.h2d_bytes += nbytes
+            if C:
+                pa_copy_blocks(self.k_pool, self.v_pool, self._view(offs, "src", torch.int32),
+                               self._view(offs, "dst", torch.int32), d_status=self.status,
+                               stream=self.stream)
+            bt = self._view(offs, "bt", torch.int32).view(S, p.table_stride)
+            abi.pa_mixed_step(self.out[:T], self.q[:T], self._view(offs, "cu", torch.int32),
+                              self._view(offs, "ctx", torch.int32), bt, self.k_pool, self.v_pool,
+                              self.scale, self.budget, k_new=self.k_new[:T], v_new=self.v_new[:T],
+                              slot_mapping=self._view(offs, "slots", torch.int64),
+                              workspace=self.ws, d_status=self.status, stream=self.stream)
         self.sched.commit()
         self.steps += 1
         return p

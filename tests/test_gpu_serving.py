@@ -39,7 +39,7 @@ def run_with_oracle(dtype, hq, hkv, d, reqs, num_blocks, budget, chunk, max_runn
         ref = oracle.paged_attention(loop.q[:T].cpu(), hk, hv,
                                      torch.from_numpy(p.cu_q_lens[:S + 1].copy()),
                                      torch.from_numpy(p.context_lens[:S].copy()),
-                                     torch.from_numpy(p.block_tables[:S].copy()), loop.scale)
+                                     torch.from_numpy(p.tables.copy()), loop.scale)
         compare(loop.out[:T], ref, dtype)
         mixed_steps += int(0 < p.num_decode < S)
     assert int(loop.status.item()) == 0

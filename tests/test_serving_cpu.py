@@ -101,10 +101,11 @@ def run_schedule(num_blocks, budget, chunk, max_running, reqs, max_ctx=4096):
         assert 0 < T <= budget and cu[-1] == T
         assert np.all(ql[:p.num_decode] == 1)          # decode tokens first
         assert np.all(ql[p.num_decode:] <= chunk)      # prefill chunks
+        assert p.table_stride == max((int(c) + B - 1) // B for c in p.context_lens[:S])
         for j in range(S):
             ctx = int(p.context_lens[j])
             nb = (ctx + B - 1) // B
-            row = p.block_tables[j]
+            row = p.tables[j]
             assert np.all(row[:nb] >= 0) and np.all(row[nb:] == -1)
             assert nb * B - ctx <= B - 1                   # paging waste bound
             for i in range(int(ql[j])):
