@@ -266,14 +266,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         mixed = run_mixed(args, dev, stream)
     extra = None
     if not args.skip_extra:
-        extra = [
-            run_decode_workload("wide_gqa_decode_bf16: 58 seqs x 4096, 16/4 heads, d 256, pool 23305",
-                                W.wide_gqa_decode(seed=args.seed), dev, stream),
-            run_decode_workload("shared_prefix_decode_bf16: 256 requests x 3 replies, 1000-token "
-                                "shared prefix + 100 unique, replies U[22,356], 32/8 heads, d 128, "
-                                "+ KV write of 768 tokens",
-                                W.shared_prefix_decode(seed=args.seed), dev, stream),
-        ]
+        extra = run_extra(args, dev, stream)
 
     serving = None
     if not args.skip_serving:
@@ -325,12 +318,36 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     return res
 
 
-def run_decode_workload(name: str, w, dev, stream, reps: int = 30) -> dict:
-    """One decode step (KV write when the workload has one, then pa_decode) on
+SHARED_PREFIX_WORKLOAD = ("shared_prefix_decode_bf16: 256 requests x 3 replies, 1000-token shared "
+                          "prefix + 100 unique, replies U[22,356], 32/8 heads, d 128, + KV write of "
+                          "768 tokens")
+
+
+def run_extra(args, dev, stream) -> list:
+    """The other decode workloads: wide-head GQA, and the shared-prefix
+    batch through pa_decode and through pa_decode_cascade (one group over the
+    62 prefix pages every sequence shares)."""
+    from paged_kv_cache_176_gb300 import workloads as W
+    w = W.wide_gqa_decode(seed=args.seed)
+    out = [run_decode_workload("wide_gqa_decode_bf16: 58 seqs x 4096, 16/4 heads, d 256, pool 23305",
+                               w, dev, stream)]
+    w = W.shared_prefix_decode(seed=args.seed)
+    out.append(run_decode_workload(SHARED_PREFIX_WORKLOAD, w, dev, stream))
+    plen = w.info["shared_pages"] * 16
+    out.append(run_decode_workload(SHARED_PREFIX_WORKLOAD + "; pa_decode_cascade, one group "
+                                   f"sharing {plen} prefix tokens", w, dev, stream,
+                                   groups=([0, w.num_seqs], [plen])))
+    return out
+
+
+def run_decode_workload(name: str, w, dev, stream, reps: int = 30, groups=None) -> dict:
+    """One decode step (KV write when the workload has one, then pa_decode, or
+    pa_decode_cascade when ``groups`` = (cu_groups, prefix_lens) is given) on
     another workload, timed with CUDA events on its stream; GB/s over the
     logical K/V bytes (every sequence's context) and over the unique bytes
-    (each physical block's filled slots counted once: shared prefix pages are
-    read from L2 after their first use)."""
+    (each physical block's filled slots counted once). A cascade also reports
+    GB/s over the bytes it has to read: each group's prefix once, plus every
+    sequence's tokens after its prefix."""
     import torch
     import paged_kv_cache_176_gb300 as pa
 
@@ -343,21 +360,35 @@ def run_decode_workload(name: str, w, dev, stream, reps: int = 30) -> dict:
             filled[bt[s][j]] = max(filled.get(bt[s][j], 0), min(16, c - 16 * j))
     logical = sum(ctx) * tok
     unique = sum(filled.values()) * tok
+    cascade_bytes = None
+    if groups is not None:
+        cu, pl = groups
+        cascade_bytes = sum(pl) * tok + sum(
+            (ctx[s] - pl[g]) * tok for g in range(len(pl)) for s in range(cu[g], cu[g + 1]))
+        cascade_bytes += sum(ctx[s] for s in range(cu[-1], len(ctx))) * tok
     with torch.cuda.stream(stream):
         d = {k: (None if getattr(w, k) is None else getattr(w, k).to(dev))
              for k in ("k_pool", "v_pool", "q", "context_lens", "block_tables", "k_new", "v_new",
                        "slot_mapping")}
         out = torch.empty_like(d["q"])
-        ws = torch.empty(pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.head_dim,
-                                                     w.max_blocks_per_seq),
+        size = pa.pa_decode_cascade_workspace_size if groups else pa.pa_decode_workspace_size
+        ws = torch.empty(size(w.num_seqs, w.num_q_heads, w.head_dim, w.max_blocks_per_seq),
                          dtype=torch.uint8, device=dev)
+        if groups is not None:
+            d_cu = torch.tensor(groups[0], dtype=torch.int32, device=dev)
+            d_pl = torch.tensor(groups[1], dtype=torch.int32, device=dev)
 
     def step():
         if d["slot_mapping"] is not None:
             pa.pa_reshape_and_cache(d["k_pool"], d["v_pool"], d["k_new"], d["v_new"],
                                     d["slot_mapping"], stream=stream)
-        pa.pa_decode(out, d["q"], d["k_pool"], d["v_pool"], d["block_tables"], d["context_lens"],
-                     w.scale, workspace=ws, stream=stream)
+        if groups is None:
+            pa.pa_decode(out, d["q"], d["k_pool"], d["v_pool"], d["block_tables"],
+                         d["context_lens"], w.scale, workspace=ws, stream=stream)
+        else:
+            pa.pa_decode_cascade(out, d["q"], d["k_pool"], d["v_pool"], d["block_tables"],
+                                 d["context_lens"], d_cu, d_pl, w.scale, workspace=ws,
+                                 stream=stream)
 
     for _ in range(5):
         step()
@@ -376,6 +407,10 @@ def run_decode_workload(name: str, w, dev, stream, reps: int = 30) -> dict:
            "unique_hbm_frac": round(unique / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
            "logical_kv_bytes": logical, "unique_kv_bytes": unique,
            "attention_tokens_per_s": round(w.num_seqs / (ms * 1e-3), 1)}
+    if cascade_bytes is not None:
+        gbs = cascade_bytes / (ms * 1e-3) / 1e9
+        res.update(cascade_kv_bytes=cascade_bytes, cascade_kv_gbs=round(gbs, 1),
+                   cascade_hbm_frac=round(gbs / pk["hbm_gbs"], 4))
     del d, out, ws
     torch.cuda.empty_cache()
     return res
@@ -645,6 +680,8 @@ def main() -> None:
                     help="skip the continuous-batching serving-loop measurement")
     ap.add_argument("--only-serving", action="store_true",
                     help="run only the serving-loop measurement (1 GPU)")
+    ap.add_argument("--only-extra", action="store_true",
+                    help="run only the other decode workloads (1 GPU)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=8.0)
     args = ap.parse_args()
@@ -660,11 +697,11 @@ def main() -> None:
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group(backend)
-    if (args.only_mixed or args.only_serving) and args.impl != "reference":
+    if (args.only_mixed or args.only_serving or args.only_extra) and args.impl != "reference":
         import torch
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
         torch.cuda.set_device(dev)
-        run = run_mixed if args.only_mixed else run_serving
+        run = run_mixed if args.only_mixed else run_serving if args.only_serving else run_extra
         res = run(args, dev, torch.cuda.Stream(dev))
     elif args.impl == "reference":
         res = run_reference(args, rank, world)

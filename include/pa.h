@@ -159,6 +159,50 @@ PA_API int pa_decode_static_ws(const pa_kv_pool* pool, void* out, const void* q,
                                int* d_status, void* stream);
 
 /*
+ * Decode over sequences that share a prompt prefix, reading the shared blocks
+ * once per group instead of once per sequence. Paging lets several sequences
+ * point their block tables at the same physical blocks: the replies of one
+ * request share its prompt's blocks ("C13 L2 serving", parallel sampling
+ * paragraph), and requests with a common prefix share its full pages by
+ * reference count ("Inference engine core techniques", section 3.2). The
+ * result is the same attention as pa_decode (up to floating-point summation
+ * order): softmax over all of a sequence's keys splits exactly into a part
+ * over the shared prefix and a part over the rest, merged through their
+ * (max, sum, accumulator) triples, the identity pa_decode's split-K uses.
+ *
+ * Groups: sequences cu_groups[g] .. cu_groups[g+1]-1 form group g; their
+ * first prefix_lens[g] tokens (a multiple of 16, at most each member's
+ * context) are held by the same physical blocks, i.e. the first
+ * prefix_lens[g]/16 entries of every member's block-table row are equal. The
+ * shared blocks are read through the group's first member's row; the caller
+ * guarantees the equality (it is not checked). Sequences outside every group,
+ * and groups with prefix_lens[g] == 0, are plain decode.
+ *
+ * Steps, all on the caller's stream: (1) one tensor-core pass per group and
+ * KV head computes the partials of every member's query rows against the
+ * shared prefix (a dense contraction: members x heads rows by prefix keys);
+ * (2) the decode kernels walk each sequence's remaining blocks and merge the
+ * prefix partial in.
+ *
+ *  cu_groups     device int32 [num_groups + 1], non-decreasing, within [0, num_seqs]
+ *  prefix_lens   device int32 [num_groups], tokens; multiple of 16
+ *  other arguments as pa_decode; workspace >= pa_decode_cascade_workspace_size()
+ *
+ * Supported: bf16 with head_dim 128 (the tensor-core prefix pass), the
+ * query/KV head ratios and KV head counts of pa_decode; otherwise
+ * PA_EUNSUPPORTED. A prefix length that is not a multiple of 16 or exceeds a
+ * member's context sets PA_STATUS_BAD_LENGTH in *d_status and that member's
+ * output row is zeros.
+ */
+PA_API size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                               int max_blocks_per_seq);
+PA_API int pa_decode_cascade(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+                             int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, const int32_t* cu_groups,
+                             const int32_t* prefix_lens, int num_groups, float scale,
+                             void* workspace, size_t workspace_bytes, int* d_status, void* stream);
+
+/*
  * Tuning knob: the number of persistent CTAs the decode kernel runs (0, the
  * default, means one per SM of the current device; values above 1024 are
  * clamped). It applies to later pa_decode / pa_mixed_step calls from any

@@ -6,6 +6,8 @@ The compute path is libpa.so (CUDA kernels behind the C ABI in include/pa.h);
 from .abi import (  # noqa: F401
     PagedAttentionError,
     pa_decode,
+    pa_decode_cascade,
+    pa_decode_cascade_workspace_size,
     pa_decode_workspace_size,
     pa_mixed_step,
     pa_mixed_workspace_size,
@@ -18,6 +20,8 @@ from .abi import (  # noqa: F401
 __all__ = [
     "pa_reshape_and_cache",
     "pa_decode",
+    "pa_decode_cascade",
+    "pa_decode_cascade_workspace_size",
     "pa_decode_workspace_size",
     "pa_mixed_step",
     "pa_mixed_workspace_size",

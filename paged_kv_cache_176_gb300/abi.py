@@ -84,6 +84,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_set_decode_ctas.argtypes = [I]
         lib.pa_decode_static_ws.restype = I
         lib.pa_decode_static_ws.argtypes = [PP, P, P, I, I, P, I, P, F, P, P]
+        lib.pa_decode_cascade_workspace_size.restype = SZ
+        lib.pa_decode_cascade_workspace_size.argtypes = [I, I, I, I]
+        lib.pa_decode_cascade.restype = I
+        lib.pa_decode_cascade.argtypes = [PP, P, P, I, I, P, I, P, P, P, I, F, P, SZ, P, P]
         _lib = lib
         return lib
 
@@ -191,6 +195,37 @@ def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale: float, 
            lib.pa_decode(ctypes.byref(pool), _ptr(out), _ptr(q), S, hq, _ptr(block_tables), mb,
                          _ptr(context_lens), float(scale), _ptr(ws), ws.numel() * ws.element_size(),
                          _ptr(d_status), _stream(stream)))
+    return out
+
+
+def pa_decode_cascade_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int,
+                                    max_blocks_per_seq: int) -> int:
+    return int(load().pa_decode_cascade_workspace_size(num_seqs, num_q_heads, head_dim,
+                                                       max_blocks_per_seq))
+
+
+def pa_decode_cascade(out, q, k_pool, v_pool, block_tables, context_lens, cu_groups, prefix_lens,
+                      scale: float, workspace=None, d_status=None, stream=None):
+    """Decode attention over groups of sequences sharing a prefix of whole
+    blocks: sequences cu_groups[g] .. cu_groups[g+1]-1 share their first
+    prefix_lens[g] tokens (see include/pa.h). q/out [S, Hq, d]. Returns out."""
+    lib = load()
+    pool = make_pool(k_pool, v_pool)
+    S, hq, d = q.shape
+    for name, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                    ("cu_groups", cu_groups), ("prefix_lens", prefix_lens)):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    ng = int(prefix_lens.shape[0])
+    if int(cu_groups.shape[0]) != ng + 1:
+        raise ValueError("cu_groups must hold num_groups + 1 entries")
+    mb = int(block_tables.shape[1])
+    ws = _workspace(pa_decode_cascade_workspace_size(S, hq, d, mb), q.device, workspace)
+    _check("pa_decode_cascade",
+           lib.pa_decode_cascade(ctypes.byref(pool), _ptr(out), _ptr(q), S, hq, _ptr(block_tables),
+                                 mb, _ptr(context_lens), _ptr(cu_groups), _ptr(prefix_lens), ng,
+                                 float(scale), _ptr(ws), ws.numel() * ws.element_size(),
+                                 _ptr(d_status), _stream(stream)))
     return out
 
 

@@ -176,6 +176,98 @@ int pa_decode(const pa_kv_pool* pool, void* out, const void* q, int num_seqs, in
   return to_status(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+// Cascade workspace: the decode workspace, then the prefix partials
+// (max, sum) [num_seqs, hq] float2 and accumulators [num_seqs, hq, head_dim] fp32.
+size_t cascade_ml_offset(int num_seqs, int num_q_heads, int head_dim) {
+  return align_up_sz(decode_workspace_bytes(num_seqs, num_q_heads, head_dim), 256);
+}
+size_t cascade_acc_offset(int num_seqs, int num_q_heads, int head_dim) {
+  return cascade_ml_offset(num_seqs, num_q_heads, head_dim) +
+         align_up_sz(static_cast<size_t>(num_seqs) * num_q_heads * 8, 256);
+}
+}  // namespace
+
+size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                        int max_blocks_per_seq) {
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0) return 0;
+  return cascade_acc_offset(num_seqs, num_q_heads, head_dim) +
+         static_cast<size_t>(num_seqs) * num_q_heads * head_dim * 4;
+}
+
+int pa_decode_cascade(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+                      int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, const int32_t* cu_groups,
+                      const int32_t* prefix_lens, int num_groups, float scale, void* workspace,
+                      size_t workspace_bytes, int* d_status, void* stream) {
+  int rc = check_pool(pool);
+  if (rc != PA_OK) return rc;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_groups < 0) return PA_EINVAL;
+  rc = check_heads(pool, num_q_heads);
+  if (rc != PA_OK) return rc;
+  const int group = num_q_heads / pool->num_kv_heads;
+  if (!decode_supported(pool->dtype, pool->head_dim, group, pool->num_kv_heads) ||
+      !prefix_supported(pool->dtype, pool->head_dim, group, num_groups))
+    return PA_EUNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (out == nullptr || q == nullptr || block_tables == nullptr || context_lens == nullptr)
+    return PA_EINVAL;
+  if (num_groups > 0 && (cu_groups == nullptr || prefix_lens == nullptr)) return PA_EINVAL;
+  if (!aligned16(out) || !aligned16(q)) return PA_EINVAL;
+  const size_t need = pa_decode_cascade_workspace_size(num_seqs, num_q_heads, pool->head_dim,
+                                                       max_blocks_per_seq);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PA_EWORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  void* pre_ml = ws + cascade_ml_offset(num_seqs, num_q_heads, pool->head_dim);
+  void* pre_acc = ws + cascade_acc_offset(num_seqs, num_q_heads, pool->head_dim);
+  if (num_groups > 0) {
+    // 1. every group's decode rows against its shared prefix, once, on the tensor cores
+    PrefillArgs pf = {};
+    pf.pool = view(pool);
+    pf.q = q;
+    pf.cu_q_lens = cu_groups;
+    pf.num_seqs = num_groups;
+    pf.num_tokens = num_seqs;
+    pf.num_q_heads = num_q_heads;
+    pf.block_tables = block_tables;
+    pf.max_blocks_per_seq = max_blocks_per_seq;
+    pf.context_lens = prefix_lens;
+    pf.scale = scale;
+    pf.d_status = d_status;
+    pf.prefix_mode = 1;
+    pf.pre_ml = pre_ml;
+    pf.pre_acc = pre_acc;
+    rc = to_status(launch_prefix_partials(pf, st));
+    if (rc != PA_OK) return rc;
+  }
+  // 2. every sequence's own blocks after its prefix, merged with the prefix partial
+  DecodeArgs a = {};
+  a.pool = view(pool);
+  a.out = out;
+  a.q = q;
+  a.cu_q_lens = nullptr;
+  a.num_seqs = num_seqs;
+  a.num_rows = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.scale = scale;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.d_status = d_status;
+  a.grid_override = g_decode_ctas.load();
+  if (num_groups > 0) {
+    a.cu_groups = cu_groups;
+    a.prefix_lens = prefix_lens;
+    a.num_groups = num_groups;
+    a.pre_ml = pre_ml;
+    a.pre_acc = pre_acc;
+  }
+  return to_status(launch_decode(a, st));
+}
+
 size_t pa_mixed_workspace_size(int num_seqs, int num_tokens, int num_q_heads, int head_dim,
                                int max_blocks_per_seq) {
   if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || head_dim <= 0 ||
@@ -225,7 +317,7 @@ int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_
     rc = to_status(launch_kv_write(w, st));
     if (rc != PA_OK) return rc;
   }
-  PrefillArgs pf;
+  PrefillArgs pf = {};
   pf.pool = view(pool);
   pf.out = out;
   pf.q = q;

@@ -136,7 +136,29 @@ struct DecodeParams {
   float* ws_acc;   // [slots, hq, D]
   int* d_status;
   SmemLayout L;
+  // cascade decode (see DecodeArgs); cu_groups == nullptr otherwise
+  const int32_t* cu_groups;
+  const int32_t* prefix_lens;
+  int num_groups;
+  const float2* pre_ml;  // [num_seqs, hq]
+  const float* pre_acc;  // [num_seqs, hq, D]
 };
+
+// Leading blocks of sequence s whose attention is already in its group's
+// shared-prefix partial (0 without groups or outside every group). A prefix
+// that is not whole blocks, or longer than the context, is flagged.
+__device__ __forceinline__ int prefix_blocks(const DecodeParams& p, int s, int ctx, bool* bad) {
+  if (p.cu_groups == nullptr || p.num_groups <= 0) return 0;
+  if (s < p.cu_groups[0] || s >= p.cu_groups[p.num_groups]) return 0;
+  const int g = upper_index(p.cu_groups, p.num_groups, s);
+  if (s >= p.cu_groups[g + 1]) return 0;
+  const int len = p.prefix_lens[g];
+  if (len < 0 || len % kBlockSize != 0 || len > ctx) {
+    *bad = true;
+    return 0;
+  }
+  return len / kBlockSize;
+}
 
 // Blocks the decode kernel reads for sequence s (0 when s is not a decode
 // sequence or its lengths are invalid).
@@ -155,7 +177,13 @@ __device__ __forceinline__ int decode_blocks(const DecodeParams& p, int s, bool*
     *bad = true;
     return 0;
   }
-  return (ctx + kBlockSize - 1) / kBlockSize;
+  bool bad_prefix = false;
+  const int skip = prefix_blocks(p, s, ctx, &bad_prefix);
+  if (bad_prefix) {
+    *bad = true;
+    return 0;
+  }
+  return (ctx + kBlockSize - 1) / kBlockSize - skip;
 }
 
 __device__ __forceinline__ int query_row(const DecodeParams& p, int s) {
@@ -246,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   const int n_cached = static_cast<int>(min(hi - lo, static_cast<int64_t>(kTableCache)));
   for (int i = tid; i < n_cached; i += kThreads) {
     const int s = upper_index(prefix, S, lo + i);
-    const int j = static_cast<int>(lo + i - prefix[s]);
+    bool unused = false;
+    const int j = static_cast<int>(lo + i - prefix[s]) + prefix_blocks(p, s, p.context_lens[s], &unused);
     table[i] = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
     block_ntok[i] = static_cast<uint8_t>(min(kBlockSize, p.context_lens[s] - j * kBlockSize));
   }
@@ -268,7 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       block_tokens = block_ntok[rel];
     } else {
       const int s = upper_index(prefix, S, lo + rel);
-      const int j = static_cast<int>(lo + rel - prefix[s]);  // logical block of sequence s
+      bool unused = false;
+      const int j = static_cast<int>(lo + rel - prefix[s]) +  // logical block of sequence s
+                    prefix_blocks(p, s, p.context_lens[s], &unused);
       phys = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
       block_tokens = min(kBlockSize, p.context_lens[s] - j * kBlockSize);
     }
@@ -317,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     const int64_t seq_units = (seq_hi - seq_lo) * parts;
     const bool whole = prefix[s] >= lo && prefix[s + 1] <= hi;
     const int row = query_row(p, s);
+    bool pre_bad = false;
+    const bool has_pre = prefix_blocks(p, s, p.context_lens[s], &pre_bad) > 0;
 
     // this lane's query heads, pre-scaled into the log2 domain
     {
@@ -546,9 +579,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     if (sub == 0 && tg == 0) {
       if (whole) {
         T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(row) * p.hq + head0) * D;
+        bool pre_poisoned[C::kGL];
+#pragma unroll
+        for (int h = 0; h < C::kGL; ++h) pre_poisoned[h] = false;
+        if (has_pre) {
+          // fold in the shared-prefix partial of this sequence
+#pragma unroll
+          for (int h = 0; h < C::kGL; ++h) {
+            const int64_t idx = static_cast<int64_t>(s) * p.hq + head0 + h;
+            const float2 pml = p.pre_ml[idx];
+            pre_poisoned[h] = pml.y < 0.f;
+            const float mn = fmaxf(m[h], pml.x);
+            const float a = merge_factor(m[h], mn), b = merge_factor(pml.x, mn);
+            l[h] = l[h] * a + pml.y * b;
+            const float* prow = p.pre_acc + idx * D;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+#pragma unroll
+              for (int i = 0; i < C::kVec / 2; ++i) {
+                const int dim = (kl + C::kLpt * c) * C::kVec + 2 * i;
+                const float2 pv = *reinterpret_cast<const float2*>(prow + dim);
+                float2& r = acc[h][c * (C::kVec / 2) + i];
+                r = make_float2(r.x * a + pv.x * b, r.y * a + pv.y * b);
+              }
+            m[h] = mn;
+          }
+        }
 #pragma unroll
         for (int h = 0; h < C::kGL; ++h) {
-          const float inv = poisoned ? 0.f : 1.f / l[h];
+          const float inv = (poisoned || pre_poisoned[h]) ? 0.f : 1.f / l[h];
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c) {
             const int dim0 = (kl + C::kLpt * c) * C::kVec;
@@ -608,11 +667,25 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
   const int* prefix = p.ws_prefix;
   const int64_t B = prefix[p.num_seqs];
   const int64_t a0 = prefix[s], a1 = prefix[s + 1];
-  if (a1 <= a0) return;
   // CTA c covers blocks [c*B/grid, (c+1)*B/grid)
-  const int64_t c_first = ((a0 + 1) * grid - 1) / B;
-  const int64_t c_last = (a1 * grid - 1) / B;
-  if (c_first == c_last) return;  // finished by the decode kernel
+  int64_t c_first = 0, c_last = -1;  // no CTA partials when the suffix is empty
+  if (a1 > a0) {
+    c_first = ((a0 + 1) * grid - 1) / B;
+    c_last = (a1 * grid - 1) / B;
+    if (c_first == c_last) return;  // finished by the decode kernel
+  } else if (p.cu_groups == nullptr) {
+    return;  // not a decode sequence, or zeroed by the decode kernel
+  }
+  bool has_pre = false;
+  if (p.cu_groups != nullptr) {
+    bool bad = false;
+    if (a1 <= a0) {
+      decode_blocks(p, s, &bad);
+      if (bad) return;  // zeroed by the decode kernel
+    }
+    has_pre = prefix_blocks(p, s, p.context_lens[s], &bad) > 0;
+    if (a1 <= a0 && !has_pre) return;
+  }
   float m = -INFINITY, l = 0.f;
   float acc[kPer];
 #pragma unroll
@@ -648,6 +721,17 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
       for (int e = 0; e < kPer; ++e) acc[e] = acc[e] * a + v[j][e] * b;
       m = mn;
     }
+  }
+  if (has_pre) {
+    const int64_t idx = static_cast<int64_t>(s) * p.hq + h;
+    const float2 pml = p.pre_ml[idx];
+    const float* src = p.pre_acc + idx * D + lane * kPer;
+    poisoned |= pml.y < 0.f;
+    const float mn = fmaxf(m, pml.x);
+    const float a = merge_factor(m, mn), b = merge_factor(pml.x, mn);
+    l = l * a + pml.y * b;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = acc[e] * a + src[e] * b;
   }
   const float inv = poisoned ? 0.f : 1.f / l;
   T* dst = static_cast<T*>(p.out) + (static_cast<int64_t>(query_row(p, s)) * p.hq + h) * D + lane * kPer;
@@ -695,6 +779,11 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   p.ws_acc = reinterpret_cast<float*>(ws + prefix_bytes + align_up_sz(slots * a.num_q_heads * 8, 256));
   p.d_status = a.d_status;
   p.L = L;
+  p.cu_groups = a.cu_groups;
+  p.prefix_lens = a.prefix_lens;
+  p.num_groups = a.num_groups;
+  p.pre_ml = static_cast<const float2*>(a.pre_ml);
+  p.pre_acc = static_cast<const float*>(a.pre_acc);
 
   auto kern = decode_kernel<T, D, G, WH>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);

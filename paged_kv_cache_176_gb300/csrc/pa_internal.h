@@ -52,6 +52,15 @@ struct DecodeArgs {
   size_t workspace_bytes;
   int* d_status;
   int grid_override;         // > 0: number of persistent CTAs (tuning / tests)
+  // shared-prefix (cascade) decode, all NULL / 0 otherwise: sequences
+  // cu_groups[g] .. cu_groups[g+1]-1 share their first prefix_lens[g] tokens
+  // (whole blocks), whose attention partials (max, sum) and fp32 accumulators
+  // are already in pre_ml [num_seqs, hq] (float2) and pre_acc [num_seqs, hq, D]
+  const int32_t* cu_groups;
+  const int32_t* prefix_lens;
+  int num_groups;
+  const void* pre_ml;
+  const void* pre_acc;
 };
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim);
 // per (dtype, head_dim) entry points, one translation unit each
@@ -78,8 +87,18 @@ struct PrefillArgs {
   const int32_t* context_lens;
   float scale;
   int* d_status;
+  // prefix mode (cascade decode): "sequence" i is group i of decode rows
+  // cu_q_lens[i] .. cu_q_lens[i+1]-1, context_lens[i] is the group's shared
+  // prefix length, its table is the row of its first member, every row sees
+  // every prefix key, and the result goes to pre_ml / pre_acc (see DecodeArgs)
+  int prefix_mode;
+  void* pre_ml;
+  void* pre_acc;
 };
 bool prefill_supported(int dtype, int head_dim, int group);
+// the tensor-core kernel in prefix mode (bf16, head_dim 128)
+bool prefix_supported(int dtype, int head_dim, int group, int num_groups);
+cudaError_t launch_prefix_partials(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 

@@ -79,6 +79,9 @@ struct TcParams {
   int64_t num_blocks;
   float scale_log2;
   int* d_status;
+  int prefix_mode;  // cascade decode: groups of decode rows over a shared prefix
+  float2* pre_ml;
+  float* pre_acc;
 };
 
 struct TcBarriers {
@@ -99,7 +102,10 @@ static_assert(sizeof(TcBarriers) <= 256, "barrier block");
 
 __device__ __forceinline__ int tc_tiles(const TcParams& p, int s, int tq) {
   const int q0 = p.cu_q_lens[s], q1 = p.cu_q_lens[s + 1];
-  if (q0 < 0 || q1 > p.num_rows || q1 - q0 <= 1) return 0;
+  // prefill: chunks of two or more rows (single rows are decode rows);
+  // prefix mode: any non-empty group with a non-empty shared prefix
+  if (q0 < 0 || q1 > p.num_rows || q1 - q0 < (p.prefix_mode ? 1 : 2)) return 0;
+  if (p.prefix_mode && p.context_lens[s] <= 0) return 0;
   return (q1 - q0 + tq - 1) / tq;
 }
 
@@ -145,15 +151,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int tok0 = tile * tq;
   const int ntok = min(tq, q_len - tok0);
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-  if (q_len > ctx || ctx > p.max_blocks * kBlockSize) {
+  const bool bad_len = p.prefix_mode ? (ctx % kBlockSize != 0 || ctx > p.max_blocks * kBlockSize)
+                                     : (q_len > ctx || ctx > p.max_blocks * kBlockSize);
+  if (bad_len) {
     if (tid == 0) status_or(p.d_status, PA_STATUS_BAD_LENGTH);
     for (int i = tid; i < ntok * G * kD; i += kThreadsTc) {
       const int tok = i / (G * kD), rem = i % (G * kD);
-      out[(static_cast<int64_t>(q0 + tok0 + tok) * p.hq + g * G) * kD + rem] = __float2bfloat16_rn(0.f);
+      const int64_t row = static_cast<int64_t>(q0 + tok0 + tok) * p.hq + g * G;
+      if (p.prefix_mode) {
+        p.pre_acc[row * kD + rem] = 0.f;
+        if (rem % kD == 0) p.pre_ml[row + rem / kD] = make_float2(0.f, -1.f);  // poisoned partial
+      } else {
+        out[row * kD + rem] = __float2bfloat16_rn(0.f);
+      }
     }
     return;
   }
-  const int max_pos = ctx - q_len + tok0 + ntok - 1;  // last row's absolute position
+  // Absolute position of the tile's first row; in prefix mode every row sits
+  // past the whole prefix (a decode token after it) and sees all its keys.
+  const int pos0 = p.prefix_mode ? ctx - 1 : ctx - q_len + tok0;
+  const int max_pos = p.prefix_mode ? pos0 : pos0 + ntok - 1;  // last row's absolute position
   const int n_kt = max_pos / kKeysTile + 1;           // key tiles
   const int nblk = max_pos / kBlockSize + 1;          // pool blocks holding keys 0..max_pos
 
@@ -191,7 +208,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   auto tile_blocks = [&](int j, int (&ph)[kBlocksTile]) -> int {
     const int b0 = j * kBlocksTile;
     const int nb = min(kBlocksTile, nblk - b0);
-    const int32_t* row = p.block_tables + static_cast<int64_t>(s) * p.max_blocks + b0;
+    // prefix mode: the shared blocks are read through the group's first member
+    const int64_t trow_idx = p.prefix_mode ? q0 : s;
+    const int32_t* row = p.block_tables + trow_idx * p.max_blocks + b0;
 #pragma unroll
     for (int b = 0; b < kBlocksTile; ++b) ph[b] = b < nb ? __ldg(row + b) : 0;
     return nb;
@@ -313,7 +332,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int hf = (warp - 2) >> 2;            // key half
     const int r = quad * 32 + lane;            // tile row owned by this thread
     const int ri = r / G;                      // token of the row within the tile
-    const int pos = ri < ntok ? ctx - q_len + tok0 + ri : -1;  // absolute position (-1: padding row)
+    const int pos = ri < ntok ? pos0 + (p.prefix_mode ? 0 : ri) : -1;  // absolute position (-1: padding row)
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t ocol = kColO + hf * kD;     // this half's O accumulator
     float m = -INFINITY, l = 0.f;
@@ -339,7 +358,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // Key halves entirely below the diagonal need no mask (every key <=
       // every row's position); the others mask keys past each row's position.
       const int key0 = j * kKeysTile + hf * kCols;
-      const bool full = key0 + kCols - 1 <= ctx - q_len + tok0 && p.scale_log2 > 0.f;
+      const bool full = key0 + kCols - 1 <= pos0 && p.scale_log2 > 0.f;
       float mx;
       {
         float mp[8];
@@ -471,6 +490,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const float mm = fmaxf(m0, m1);
         const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mm);
         const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mm);
+        if (p.prefix_mode) {
+          // the unnormalised partial (max mm, sum, accumulator) of this row
+          const int64_t idx = static_cast<int64_t>(q0 + tok0 + ri) * p.hq + g * G + rh;
+          float* arow = p.pre_acc + idx * kD + hf * 64;
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              float x[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                x[k] = __uint_as_float(raw[0][c][e + k]) * a0 + __uint_as_float(raw[1][c][e + k]) * a1;
+              *reinterpret_cast<float4*>(arow + c * 32 + e) = make_float4(x[0], x[1], x[2], x[3]);
+            }
+          if (hf == 0) p.pre_ml[idx] = make_float2(mm, bar.bad_block ? -1.f : a0 * l0 + a1 * l1);
+        } else {
         const float inv = bar.bad_block ? 0.f : 1.f / (a0 * l0 + a1 * l1);
         const float s0 = a0 * inv, s1 = a1 * inv;
         __nv_bfloat16* orow =
@@ -490,6 +525,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             }
             *reinterpret_cast<uint4*>(orow + c * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
           }
+        }
       }
     } else if (r == 0 && hf == 0) {
       status_or(p.d_status, PA_STATUS_TIMEOUT);
@@ -568,6 +604,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   p.num_blocks = a.pool.num_blocks;
   p.scale_log2 = a.scale * kLog2e;
   p.d_status = a.d_status;
+  p.prefix_mode = a.prefix_mode;
+  p.pre_ml = static_cast<float2*>(a.pre_ml);
+  p.pre_acc = static_cast<float*>(a.pre_acc);
   const int tq_tokens = kRowsTile / group;
   const int tiles = (a.num_tokens + tq_tokens - 1) / tq_tokens + a.num_seqs;  // upper bound
   const int smem = kSmemTc;
@@ -580,6 +619,17 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+bool prefix_supported(int dtype, int head_dim, int group, int num_groups) {
+  return dtype == PA_BF16 && head_dim == kD && group >= 1 && group <= 8 && kRowsTile % group == 0 &&
+         num_groups <= kMaxPrefixSeqs && encode_tiled() != nullptr;
+}
+
+cudaError_t launch_prefix_partials(const PrefillArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0 || a.num_tokens == 0) return cudaSuccess;
+  if (!a.prefix_mode || a.pre_ml == nullptr || a.pre_acc == nullptr) return cudaErrorInvalidValue;
+  return launch_prefill_tc(a, stream);
+}
 
 bool prefill_supported(int dtype, int head_dim, int group) {
   if (dtype != PA_F32 && dtype != PA_BF16) return false;

@@ -462,6 +462,29 @@ def shared_prefix_decode(seed: int = 0, num_requests: int = 256, replies: int = 
     )
 
 
+
+def share_prefix(w: Workload, cu_groups: Sequence[int], prefix_lens: Sequence[int]) -> Workload:
+    """The same workload with shared prompt prefixes: the members
+    ``cu_groups[g] .. cu_groups[g+1]-1`` of group ``g`` point the first
+    ``prefix_lens[g] // 16`` entries of their block tables at the first
+    member's blocks (the blocks they gave up stay in the pool, unreferenced).
+    Each prefix must fit every member's context. Structure only: the values
+    in the pool are untouched."""
+    b = w.block_size
+    bt = w.block_tables.clone()
+    ctx = w.context_lens
+    for g in range(len(prefix_lens)):
+        a, e, plen = int(cu_groups[g]), int(cu_groups[g + 1]), int(prefix_lens[g])
+        nb = plen // b
+        for s in range(a + 1, e):
+            assert plen <= int(ctx[s]) and plen <= int(ctx[a])
+            bt[s, :nb] = bt[a, :nb]
+    info = dict(w.info)
+    info.update(cu_groups=[int(x) for x in cu_groups], prefix_lens=[int(x) for x in prefix_lens])
+    return Workload(w.name + "+shared", w.dtype, w.num_q_heads, w.num_kv_heads, w.head_dim, b,
+                    w.k_pool, w.v_pool, w.q, w.cu_q_lens, w.context_lens, bt, w.k_new, w.v_new,
+                    w.slot_mapping, w.scale, w.token_budget, info)
+
 CONFIGS = {
     "tiny_decode_f32": tiny_decode_f32,
     "decode_b64_bf16": decode_b64,

@@ -109,3 +109,22 @@ def test_binding_rejects_host_tensors():
     k = torch.zeros(4, 16, 2, 64)
     with pytest.raises(ValueError):
         abi.make_pool(k, k)
+
+
+def cascade(lib, pl, S=4, hq=8, mb=8, ng=1, cu=FAKE, plen=FAKE, ws=FAKE, ws_bytes=1 << 40):
+    return lib.pa_decode_cascade(ctypes.byref(pl), FAKE, FAKE, S, hq, FAKE, mb, FAKE, cu, plen, ng,
+                                 0.125, ws, ws_bytes, None, None)
+
+
+def test_cascade_validation(lib):
+    bf16 = dict(dtype=1, head_dim=128)
+    assert cascade(lib, pool(k=None, **bf16)) == abi.PA_EINVAL
+    assert cascade(lib, pool(**bf16), ng=-1) == abi.PA_EINVAL
+    assert cascade(lib, pool(**bf16), mb=0) == abi.PA_EINVAL
+    assert cascade(lib, pool(**bf16), hq=7) == abi.PA_EINVAL          # heads not a multiple
+    # the shared-prefix pass runs on the bf16 head_dim-128 tensor-core kernel only
+    assert cascade(lib, pool(dtype=0, head_dim=128)) == abi.PA_EUNSUPPORTED
+    assert cascade(lib, pool(dtype=1, head_dim=64)) == abi.PA_EUNSUPPORTED
+    sz = abi.pa_decode_cascade_workspace_size(768, 32, 128, 100)
+    assert sz > abi.pa_decode_workspace_size(768, 32, 128, 100) + 768 * 32 * 128 * 4
+    assert abi.pa_decode_cascade_workspace_size(-1, 32, 128, 100) == 0
