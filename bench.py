@@ -337,7 +337,68 @@ def run_extra(args, dev, stream) -> list:
     out.append(run_decode_workload(SHARED_PREFIX_WORKLOAD + "; pa_decode_cascade, one group "
                                    f"sharing {plen} prefix tokens", w, dev, stream,
                                    groups=([0, w.num_seqs], [plen])))
+    del w
+    out.append(run_cow_step(args, dev, stream))
     return out
+
+
+def run_cow_step(args, dev, stream, reps: int = 200) -> dict:
+    """The copy-on-write step of the shared-prefix workload: each request's
+    last prompt block (12 filled slots) is copied for two of its three
+    replies (512 pairs) and the 768 new tokens are written. Fused
+    (pa_reshape_and_cache_cow: one launch, filled slots only) against the
+    separate pa_copy_blocks (whole blocks) + pa_reshape_and_cache."""
+    import torch
+    import paged_kv_cache_176_gb300 as pa
+    from paged_kv_cache_176_gb300 import workloads as W
+    from paged_kv_cache_176_gb300.serving import pa_copy_blocks, pa_reshape_and_cache_cow
+
+    w = W.shared_prefix_decode(seed=args.seed)
+    R, rep = w.info["num_requests"], w.info["replies"]
+    prompt = 1100
+    j, ntok = prompt // 16, prompt % 16
+    bt = w.block_tables
+    src = [int(bt[r * rep + rep - 1, j]) for r in range(R) for _ in range(rep - 1)]
+    dst = [int(bt[r * rep + k, j]) for r in range(R) for k in range(rep - 1)]
+    tok = 2 * w.num_kv_heads * w.head_dim * w.k_pool.element_size()
+    fused_bytes = 2 * len(src) * ntok * tok + 2 * w.num_seqs * tok + 8 * w.num_seqs + 12 * len(src)
+    with torch.cuda.stream(stream):
+        kp, vp = w.k_pool.to(dev), w.v_pool.to(dev)
+        kn, vn, sm = w.k_new.to(dev), w.v_new.to(dev), w.slot_mapping.to(dev)
+        d_src = torch.tensor(src, dtype=torch.int32, device=dev)
+        d_dst = torch.tensor(dst, dtype=torch.int32, device=dev)
+        d_n = torch.full((len(src),), ntok, dtype=torch.int32, device=dev)
+
+    def fused():
+        pa_reshape_and_cache_cow(kp, vp, kn, vn, sm, d_src, d_dst, d_n, stream=stream)
+
+    def separate():
+        pa_copy_blocks(kp, vp, d_src, d_dst, stream=stream)
+        pa.pa_reshape_and_cache(kp, vp, kn, vn, sm, stream=stream)
+
+    def timed(fn):
+        for _ in range(10):
+            fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps * 1e3
+
+    us_f, us_s = timed(fused), timed(separate)
+    pk = peaks()
+    gbs = fused_bytes / (us_f * 1e-6) / 1e9
+    del kp, vp
+    torch.cuda.empty_cache()
+    return {"workload": f"shared-prefix copy-on-write step: {len(src)} pairs x {ntok} filled slots "
+                        f"+ {w.num_seqs} new tokens, 8 KV heads, d 128, bf16",
+            "fused_us": round(us_f, 2), "separate_us": round(us_s, 2),
+            "fused_bytes": fused_bytes, "fused_gbs": round(gbs, 1),
+            "fused_hbm_frac": round(gbs / pk["hbm_gbs"], 4), "launches_fused": 1,
+            "launches_separate": 2}
 
 
 def run_decode_workload(name: str, w, dev, stream, reps: int = 30, groups=None) -> dict:

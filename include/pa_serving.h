@@ -60,11 +60,28 @@ PA_API int pa_bm_fork(pa_block_manager* bm, int64_t parent, int64_t child);
  * (block * block_size + offset) of the i-th new token. If the last block is
  * shared and partially filled it is first replaced by a fresh copy: the
  * (source, destination) block pair is written to cow_src/cow_dst (capacity 1
- * is enough) and *n_cow is set to the number of pairs; the caller copies the
- * block on the device (pa_copy_blocks) before writing the new tokens.
+ * is enough), the number of filled slots to copy to cow_ntok (nullable), and
+ * *n_cow is set to the number of pairs. The caller copies the filled slots on
+ * the device (pa_reshape_and_cache_cow, fused with the token writes, or
+ * pa_copy_blocks) before the attention reads the block.
  */
 PA_API int pa_bm_append(pa_block_manager* bm, int64_t seq, int n, int64_t* slots_out,
-                        int32_t* cow_src, int32_t* cow_dst, int* n_cow);
+                        int32_t* cow_src, int32_t* cow_dst, int32_t* cow_ntok, int* n_cow);
+
+/*
+ * One beam-search step ("Inference engine core techniques", section 1.5: the
+ * beams share their prefix pages and copy only where they diverge). New beam
+ * i continues old beam old_ids[parents[i]]: it shares every block of that
+ * beam (reference counts + 1); then every old beam is released, so the
+ * blocks of beams that left no child return to the pool. A new id may reuse
+ * an old beam's id. The next pa_bm_append of each new beam copies a shared
+ * partial last block (copy-on-write); the last holder writes in place.
+ * PA_EINVAL (nothing changed) on unknown or repeated old ids, a parent index
+ * outside [0, n_old), repeated new ids, or a new id held by a live sequence
+ * that is not an old beam.
+ */
+PA_API int pa_bm_beam_step(pa_block_manager* bm, int n_old, const int64_t* old_ids, int n_new,
+                           const int32_t* parents, const int64_t* new_ids);
 
 /* Release seq: blocks whose count reaches zero return to the pool. */
 PA_API int pa_bm_free(pa_block_manager* bm, int64_t seq);
@@ -105,6 +122,7 @@ typedef struct {
   int64_t* slot_mapping;  /* [max_tokens] */
   int32_t* cow_src;       /* [max_cow] blocks to copy before the KV write */
   int32_t* cow_dst;       /* [max_cow] */
+  int32_t* cow_ntok;      /* [max_cow] filled slots of cow_src to copy (nullable) */
 } pa_step_plan;
 
 /* Build the next step (removing finished sequences, admitting requests,
@@ -127,6 +145,24 @@ PA_API int pa_sched_stats(const pa_scheduler* s, int64_t* waiting, int64_t* runn
  */
 PA_API int pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src, const int32_t* dst, int n,
                           int* d_status, void* stream);
+
+/*
+ * The KV write of a step (pa_reshape_and_cache) and its copy-on-write copies
+ * in one launch: for i < n_cow the first cow_ntok[i] token slots of block
+ * cow_src[i] are copied onto block cow_dst[i] (only the filled part of the
+ * shared block, not all 16 slots), and token t is written to slot
+ * slot_mapping[t] (-1 skips). The new tokens that land in a copied block must
+ * sit at offsets >= its cow_ntok, which pa_bm_append guarantees: the copies
+ * and the writes then touch disjoint slots and need no ordering. A pair with
+ * a block outside the pool or cow_ntok outside [0, 16] sets
+ * PA_STATUS_BAD_BLOCK and is skipped; a slot outside the pool sets
+ * PA_STATUS_BAD_SLOT. cow_* are device int32 arrays.
+ */
+PA_API int pa_reshape_and_cache_cow(const pa_kv_pool* pool, const void* k_new, const void* v_new,
+                                    const int64_t* slot_mapping, int num_tokens,
+                                    const int32_t* cow_src, const int32_t* cow_dst,
+                                    const int32_t* cow_ntok, int n_cow, int* d_status,
+                                    void* stream);
 
 #ifdef __cplusplus
 }

@@ -60,6 +60,50 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_
   }
 }
 
+// One launch for a step's KV write and its copy-on-write copies. CTAs
+// 0 .. num_tokens-1 write one new token each (as kv_write_kernel); CTA
+// num_tokens + i copies the first ntok[i] token slots of block src[i] onto
+// block dst[i], the filled part of a shared block that is about to receive
+// new tokens at offsets >= ntok[i]. The copies and the writes touch disjoint
+// slots, so they need no ordering inside the launch.
+__global__ void __launch_bounds__(128) kv_write_cow_kernel(
+    uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, int64_t num_blocks, int vecs_per_token,
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+    const int64_t* __restrict__ slot_mapping, int num_tokens, const int32_t* __restrict__ src,
+    const int32_t* __restrict__ dst, const int32_t* __restrict__ ntok, int* d_status) {
+  const int b = blockIdx.x;
+  if (b < num_tokens) {
+    const int64_t slot = slot_mapping[b];
+    if (slot < 0) return;  // padding token
+    if (slot >= num_blocks * kBlockSize) {
+      if (threadIdx.x == 0) status_or(d_status, PA_STATUS_BAD_SLOT);
+      return;
+    }
+    const int64_t dst_v = slot * vecs_per_token;
+    const int64_t src_v = static_cast<int64_t>(b) * vecs_per_token;
+    for (int i = threadIdx.x; i < vecs_per_token; i += blockDim.x) {
+      const uint4 kv = __ldg(k_new + src_v + i);
+      const uint4 vv = __ldg(v_new + src_v + i);
+      k_pool[dst_v + i] = kv;
+      v_pool[dst_v + i] = vv;
+    }
+    return;
+  }
+  const int i = b - num_tokens;
+  const int64_t s = src[i], d = dst[i];
+  const int n = ntok[i];
+  if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks || n < 0 || n > kBlockSize) {
+    if (threadIdx.x == 0) status_or(d_status, PA_STATUS_BAD_BLOCK);
+    return;
+  }
+  const int vecs = n * vecs_per_token;
+  const int64_t so = s * kBlockSize * vecs_per_token, dof = d * kBlockSize * vecs_per_token;
+  for (int v = threadIdx.x; v < vecs; v += blockDim.x) {
+    k_pool[dof + v] = k_pool[so + v];
+    v_pool[dof + v] = v_pool[so + v];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream) {
@@ -92,6 +136,37 @@ extern "C" int pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src, const 
   pa::copy_blocks_kernel<<<n, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<uint4*>(pool->k), static_cast<uint4*>(pool->v), pool->num_blocks,
       static_cast<int>(bytes / 16), src, dst, d_status);
+  if (cudaGetLastError() != cudaSuccess) return PA_ECUDA;
+  return PA_OK;
+}
+
+extern "C" int pa_reshape_and_cache_cow(const pa_kv_pool* pool, const void* k_new,
+                                        const void* v_new, const int64_t* slot_mapping,
+                                        int num_tokens, const int32_t* cow_src,
+                                        const int32_t* cow_dst, const int32_t* cow_ntok,
+                                        int n_cow, int* d_status, void* stream) {
+  if (pool == nullptr || pool->k == nullptr || pool->v == nullptr || num_tokens < 0 || n_cow < 0)
+    return PA_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(pool->k) & 15u) || (reinterpret_cast<uintptr_t>(pool->v) & 15u))
+    return PA_EINVAL;
+  if (pool->num_blocks <= 0 || pool->num_kv_heads <= 0 || pool->head_dim <= 0) return PA_EINVAL;
+  if (pool->block_size != pa::kBlockSize) return PA_EUNSUPPORTED;
+  if (pool->dtype != PA_F32 && pool->dtype != PA_BF16) return PA_EUNSUPPORTED;
+  const int64_t elt = pool->dtype == PA_BF16 ? 2 : 4;
+  const int64_t token_bytes = static_cast<int64_t>(pool->num_kv_heads) * pool->head_dim * elt;
+  if (token_bytes % 16 != 0) return PA_EUNSUPPORTED;
+  if (num_tokens > 0) {
+    if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return PA_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(k_new) & 15u) || (reinterpret_cast<uintptr_t>(v_new) & 15u))
+      return PA_EINVAL;
+  }
+  if (n_cow > 0 && (cow_src == nullptr || cow_dst == nullptr || cow_ntok == nullptr)) return PA_EINVAL;
+  if (num_tokens + n_cow == 0) return PA_OK;
+  const int vecs = static_cast<int>(token_bytes / 16);
+  pa::kv_write_cow_kernel<<<num_tokens + n_cow, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(pool->k), static_cast<uint4*>(pool->v), pool->num_blocks, vecs,
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, num_tokens,
+      cow_src, cow_dst, cow_ntok, d_status);
   if (cudaGetLastError() != cudaSuccess) return PA_ECUDA;
   return PA_OK;
 }

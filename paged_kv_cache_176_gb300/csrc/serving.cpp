@@ -4,6 +4,7 @@
 #include <deque>
 #include <new>
 #include <unordered_map>
+#include <unordered_set>
 #include <vector>
 
 #include "../../include/pa_serving.h"
@@ -75,7 +76,7 @@ int pa_bm_fork(pa_block_manager* bm, int64_t parent, int64_t child) {
 }
 
 int pa_bm_append(pa_block_manager* bm, int64_t seq, int n, int64_t* slots_out, int32_t* cow_src,
-                 int32_t* cow_dst, int* n_cow) {
+                 int32_t* cow_dst, int32_t* cow_ntok, int* n_cow) {
   if (bm == nullptr || n < 0 || (n > 0 && slots_out == nullptr)) return PA_EINVAL;
   auto it = bm->seqs.find(seq);
   if (it == bm->seqs.end()) return PA_EINVAL;
@@ -94,6 +95,7 @@ int pa_bm_append(pa_block_manager* bm, int64_t seq, int n, int64_t* slots_out, i
     s.blocks.back() = fresh;
     cow_src[0] = old;
     cow_dst[0] = fresh;
+    if (cow_ntok != nullptr) cow_ntok[0] = static_cast<int32_t>(s.tokens % b);
     *n_cow = 1;
   }
   for (int i = 0; i < n; ++i) {
@@ -102,6 +104,33 @@ int pa_bm_append(pa_block_manager* bm, int64_t seq, int n, int64_t* slots_out, i
     slots_out[i] = static_cast<int64_t>(s.blocks[pos / b]) * b + pos % b;
   }
   s.tokens += n;
+  return PA_OK;
+}
+
+int pa_bm_beam_step(pa_block_manager* bm, int n_old, const int64_t* old_ids, int n_new,
+                    const int32_t* parents, const int64_t* new_ids) {
+  if (bm == nullptr || n_old < 0 || n_new < 0) return PA_EINVAL;
+  if ((n_old > 0 && old_ids == nullptr) || (n_new > 0 && (parents == nullptr || new_ids == nullptr)))
+    return PA_EINVAL;
+  // check everything first so that a rejected call changes nothing
+  std::unordered_set<int64_t> olds, news;
+  for (int i = 0; i < n_old; ++i)
+    if (!bm->seqs.count(old_ids[i]) || !olds.insert(old_ids[i]).second) return PA_EINVAL;
+  for (int i = 0; i < n_new; ++i) {
+    if (parents[i] < 0 || parents[i] >= n_old) return PA_EINVAL;
+    if (!news.insert(new_ids[i]).second) return PA_EINVAL;
+    if (bm->seqs.count(new_ids[i]) && !olds.count(new_ids[i])) return PA_EINVAL;
+  }
+  // children share every block of their parent; then the old beams leave.
+  // Children are built aside first, as a new id may reuse an old beam's id.
+  std::vector<pa_block_manager::Seq> kids;
+  kids.reserve(static_cast<size_t>(n_new));
+  for (int i = 0; i < n_new; ++i) {
+    kids.push_back(bm->seqs.at(old_ids[parents[i]]));
+    for (int32_t b : kids.back().blocks) ++bm->refcount[b];
+  }
+  for (int i = 0; i < n_old; ++i) pa_bm_free(bm, old_ids[i]);
+  for (int i = 0; i < n_new; ++i) bm->seqs.emplace(new_ids[i], std::move(kids[static_cast<size_t>(i)]));
   return PA_OK;
 }
 
@@ -267,15 +296,16 @@ int pa_sched_step(pa_scheduler* s, pa_step_plan* plan) {
   int64_t t = 0;
   for (size_t j = 0; j < order.size(); ++j) {
     const auto& r = s->running[order[j]];
-    int32_t src = -1, dst = -1;
+    int32_t src = -1, dst = -1, ntok = 0;
     int n_cow = 0;
     const int rc = pa_bm_append(bm, r.id, static_cast<int>(r.step_n), plan->slot_mapping + t, &src,
-                                &dst, &n_cow);
+                                &dst, &ntok, &n_cow);
     if (rc != PA_OK) return rc;  // cannot happen: admission reserved the blocks
     if (n_cow > 0) {
       if (plan->num_cow >= plan->max_cow) return PA_EINVAL;
       plan->cow_src[plan->num_cow] = src;
       plan->cow_dst[plan->num_cow] = dst;
+      if (plan->cow_ntok != nullptr) plan->cow_ntok[plan->num_cow] = ntok;
       ++plan->num_cow;
     }
     t += r.step_n;

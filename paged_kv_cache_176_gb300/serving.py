@@ -3,9 +3,9 @@
 ``BlockManager`` and ``Scheduler`` are ctypes bindings of the native C++
 objects (argument marshalling only). ``ServingLoop`` drives them: every step
 it asks the scheduler for a batch (decode tokens first, then prefill chunks
-under the token budget), copies the plan to the device, runs the
-copy-on-write block copies and one ``pa_mixed_step`` (the step's KV write
-fused in) over the paged pool, then commits the step. There is no model: the
+under the token budget), copies the plan to the device, runs the step's KV
+write (fused with its copy-on-write copies when the step has any) and one
+``pa_mixed_step`` over the paged pool, then commits the step. There is no model: the
 new tokens' q/k/v are seeded random values, which is all the attention path
 needs.
 """
@@ -32,7 +32,7 @@ class _Plan(ctypes.Structure):
         ("seq_ids", ctypes.c_void_p), ("cu_q_lens", ctypes.c_void_p),
         ("context_lens", ctypes.c_void_p), ("block_tables", ctypes.c_void_p),
         ("slot_mapping", ctypes.c_void_p), ("cow_src", ctypes.c_void_p),
-        ("cow_dst", ctypes.c_void_p),
+        ("cow_dst", ctypes.c_void_p), ("cow_ntok", ctypes.c_void_p),
     ]
 
 
@@ -55,7 +55,9 @@ def _lib() -> ctypes.CDLL:
         lib.pa_bm_fork.restype = I
         lib.pa_bm_fork.argtypes = [P, I64, I64]
         lib.pa_bm_append.restype = I
-        lib.pa_bm_append.argtypes = [P, I64, I, P, P, P, P]
+        lib.pa_bm_append.argtypes = [P, I64, I, P, P, P, P, P]
+        lib.pa_bm_beam_step.restype = I
+        lib.pa_bm_beam_step.argtypes = [P, I, P, I, P, P]
         lib.pa_bm_free.restype = I
         lib.pa_bm_free.argtypes = [P, I64]
         lib.pa_bm_num_tokens.restype = I64
@@ -78,6 +80,9 @@ def _lib() -> ctypes.CDLL:
         lib.pa_sched_stats.argtypes = [P, P, P, P, P, P]
         lib.pa_copy_blocks.restype = I
         lib.pa_copy_blocks.argtypes = [ctypes.POINTER(abi.pa_kv_pool), P, P, I, P, P]
+        lib.pa_reshape_and_cache_cow.restype = I
+        lib.pa_reshape_and_cache_cow.argtypes = [ctypes.POINTER(abi.pa_kv_pool), P, P, P, I, P, P,
+                                                 P, I, P, P]
         _ready = True
     return lib
 
@@ -114,16 +119,29 @@ class BlockManager:
         abi._check("pa_bm_fork", self._lib.pa_bm_fork(self._h, parent, child))
 
     def append(self, seq: int, n: int):
-        """Slots of n new tokens and the copy-on-write pairs [(src, dst)]."""
+        """Slots of n new tokens and the copy-on-write pairs
+        [(src, dst, filled slots to copy)]."""
         slots = np.empty(max(n, 1), dtype=np.int64)
         src = np.empty(1, dtype=np.int32)
         dst = np.empty(1, dtype=np.int32)
+        ntok = np.empty(1, dtype=np.int32)
         n_cow = ctypes.c_int(0)
         rc = self._lib.pa_bm_append(self._h, seq, n, _np_ptr(slots), _np_ptr(src), _np_ptr(dst),
-                                    ctypes.byref(n_cow))
+                                    _np_ptr(ntok), ctypes.byref(n_cow))
         abi._check("pa_bm_append", rc)
-        cow = [(int(src[0]), int(dst[0]))] if n_cow.value else []
+        cow = [(int(src[0]), int(dst[0]), int(ntok[0]))] if n_cow.value else []
         return slots[:n], cow
+
+    def beam_step(self, old_ids, parents, new_ids) -> None:
+        """New beam i continues old beam old_ids[parents[i]] (shared blocks);
+        the old beams are released."""
+        old = np.ascontiguousarray(old_ids, dtype=np.int64)
+        par = np.ascontiguousarray(parents, dtype=np.int32)
+        new = np.ascontiguousarray(new_ids, dtype=np.int64)
+        if par.size != new.size:
+            raise ValueError("one parent per new beam")
+        abi._check("pa_bm_beam_step", self._lib.pa_bm_beam_step(
+            self._h, old.size, _np_ptr(old), new.size, _np_ptr(par), _np_ptr(new)))
 
     def free(self, seq: int) -> None:
         abi._check("pa_bm_free", self._lib.pa_bm_free(self._h, seq))
@@ -153,11 +171,12 @@ class StepPlan:
         self.slot_mapping = np.zeros(max_tokens, dtype=np.int64)
         self.cow_src = np.zeros(max_cow, dtype=np.int32)
         self.cow_dst = np.zeros(max_cow, dtype=np.int32)
+        self.cow_ntok = np.zeros(max_cow, dtype=np.int32)
         self.c = _Plan(max_seqs, max_tokens, max_blocks_per_seq, max_cow, 0, 0, 0, 0, 0,
                        _np_ptr(self.seq_ids).value, _np_ptr(self.cu_q_lens).value,
                        _np_ptr(self.context_lens).value, _np_ptr(self.block_tables).value,
                        _np_ptr(self.slot_mapping).value, _np_ptr(self.cow_src).value,
-                       _np_ptr(self.cow_dst).value)
+                       _np_ptr(self.cow_dst).value, _np_ptr(self.cow_ntok).value)
 
     @property
     def num_seqs(self) -> int:
@@ -221,6 +240,21 @@ class Scheduler:
         return {k: int(x.value) for k, x in zip(keys, v)}
 
 
+def pa_reshape_and_cache_cow(k_pool, v_pool, k_new, v_new, slot_mapping, cow_src, cow_dst,
+                             cow_ntok, d_status=None, stream=None) -> None:
+    """KV write of the step's tokens with the copy-on-write copies (the filled
+    slots of shared blocks) fused into the same launch."""
+    lib = _lib()
+    pool = abi.make_pool(k_pool, v_pool)
+    T = 0 if slot_mapping is None else int(slot_mapping.numel())
+    n = 0 if cow_src is None else int(cow_src.numel())
+    abi._check("pa_reshape_and_cache_cow",
+               lib.pa_reshape_and_cache_cow(ctypes.byref(pool), abi._ptr(k_new), abi._ptr(v_new),
+                                            abi._ptr(slot_mapping), T, abi._ptr(cow_src),
+                                            abi._ptr(cow_dst), abi._ptr(cow_ntok), n,
+                                            abi._ptr(d_status), abi._stream(stream)))
+
+
 def pa_copy_blocks(k_pool, v_pool, src: torch.Tensor, dst: torch.Tensor, d_status=None,
                    stream=None) -> None:
     """Device copy of whole K/V blocks src[i] -> dst[i] (copy-on-write)."""
@@ -274,9 +308,9 @@ class ServingLoop:
         self.v_new = torch.empty_like(self.k_new)
         self.out = torch.empty_like(self.q)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
-        # packed plan: slots (int64) | cu (S+1) | ctx (S) | cow src | cow dst | tables
+        # packed plan: slots (int64) | cu (S+1) | ctx (S) | cow src | dst | ntok | tables
         self._cap = (_align16(8 * T) + _align16(4 * (S + 1)) + _align16(4 * S) +
-                     2 * _align16(4 * max_cow) + _align16(4 * S * mb))
+                     3 * _align16(4 * max_cow) + _align16(4 * S * mb))
         self._dev = torch.empty(self._cap, dtype=torch.uint8, device=self.device)
         self._host = [torch.empty(self._cap, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
         self._host_np = [h.numpy() for h in self._host]
@@ -313,6 +347,7 @@ class ServingLoop:
                               ("ctx", p.context_lens[:S], np.int32),
                               ("src", p.cow_src[:C], np.int32),
                               ("dst", p.cow_dst[:C], np.int32),
+                              ("ntok", p.cow_ntok[:C], np.int32),
                               ("bt", p.block_tables[:S * W], np.int32)):
             n = src.size * np.dtype(dt).itemsize
             buf[o:o + n].view(dt)[:] = src
@@ -343,15 +378,22 @@ class ServingLoop:
             self._sent[k] = ev
             self._k ^= 1
             self.h2d_bytes += nbytes
-            if C:
-                pa_copy_blocks(self.k_pool, self.v_pool, self._view(offs, "src", torch.int32),
-                               self._view(offs, "dst", torch.int32), d_status=self.status,
-                               stream=self.stream)
+            slots = self._view(offs, "slots", torch.int64)
             bt = self._view(offs, "bt", torch.int32).view(S, p.table_stride)
+            if C:
+                # copy-on-write copies fused with the step's KV write
+                pa_reshape_and_cache_cow(self.k_pool, self.v_pool, self.k_new[:T], self.v_new[:T],
+                                         slots, self._view(offs, "src", torch.int32),
+                                         self._view(offs, "dst", torch.int32),
+                                         self._view(offs, "ntok", torch.int32),
+                                         d_status=self.status, stream=self.stream)
+            write = C == 0  # otherwise already written above
             abi.pa_mixed_step(self.out[:T], self.q[:T], self._view(offs, "cu", torch.int32),
                               self._view(offs, "ctx", torch.int32), bt, self.k_pool, self.v_pool,
-                              self.scale, self.budget, k_new=self.k_new[:T], v_new=self.v_new[:T],
-                              slot_mapping=self._view(offs, "slots", torch.int64),
+                              self.scale, self.budget,
+                              k_new=self.k_new[:T] if write else None,
+                              v_new=self.v_new[:T] if write else None,
+                              slot_mapping=slots if write else None,
                               workspace=self.ws, d_status=self.status, stream=self.stream)
         self.sched.commit()
         self.steps += 1

@@ -35,7 +35,7 @@ def test_fork_shares_and_copy_on_write():
     bm.fork(1, 2)                         # parallel sampling: reply 2 shares the prompt
     assert bm.refcount(b0) == 2 and bm.refcount(b1) == 2 and bm.num_free == 6
     slots, cow = bm.append(2, 1)          # first write into the shared partial block
-    assert len(cow) == 1 and cow[0][0] == b1
+    assert len(cow) == 1 and cow[0][0] == b1 and cow[0][2] == 4  # 4 filled slots to copy
     fresh = cow[0][1]
     assert list(bm.block_table(2)) == [b0, fresh]
     assert bm.refcount(b1) == 1 and bm.refcount(fresh) == 1 and bm.refcount(b0) == 2
@@ -58,6 +58,51 @@ def test_full_shared_block_needs_no_copy():
     bm.fork(1, 2)
     slots, cow = bm.append(2, 3)
     assert cow == [] and len(bm.block_table(2)) == 2
+
+
+def test_beam_step_shares_prunes_and_copies_on_write():
+    bm = BlockManager(16, B)
+    bm.add(1)
+    bm.append(1, 20)                                   # prompt: b0 full, b1 holds 4
+    b0, b1 = bm.block_table(1)
+    bm.beam_step([1], [0, 0, 0, 0], [10, 11, 12, 13])  # 4 beams from the prompt
+    assert bm.num_tokens(1) == -1 and bm.refcount(b0) == 4 and bm.refcount(b1) == 4
+    assert bm.num_free == 14
+    cows = [bm.append(beam, 1)[1] for beam in (10, 11, 12, 13)]
+    # the first three writers copy the shared partial block (4 filled slots),
+    # the last one finds it unshared and writes in place
+    assert [len(c) for c in cows] == [1, 1, 1, 0]
+    assert all(c[0][0] == b1 and c[0][2] == 4 for c in cows[:3])
+    assert bm.block_table(13)[1] == b1 and bm.num_free == 11
+    own = {beam: int(bm.block_table(beam)[1]) for beam in (10, 11, 12, 13)}
+    # beam 11 leaves no child; beam 10 has two
+    bm.beam_step([10, 11, 12, 13], [0, 0, 2, 3], [20, 21, 22, 23])
+    assert bm.refcount(own[11]) == 0 and bm.refcount(own[10]) == 2 and bm.num_free == 12
+    assert bm.refcount(b0) == 4
+    # ids may be reused across steps
+    bm.beam_step([20, 21, 22, 23], [3, 2, 1, 0], [20, 21, 22, 23])
+    assert bm.refcount(own[10]) == 2 and bm.num_free == 12
+    for beam in (20, 21, 22, 23):
+        bm.free(beam)
+    assert bm.num_free == 16 and all(bm.refcount(b) == 0 for b in range(16))
+
+
+def test_beam_step_rejects_and_changes_nothing():
+    bm = BlockManager(8, B)
+    for sq in (1, 2):
+        bm.add(sq)
+        bm.append(sq, 17)
+    bm.add(9)
+    before = (bm.num_free, [bm.refcount(b) for b in range(8)])
+    for old, par, new in (([1, 2], [0, 2], [5, 6]),     # parent index out of range
+                          ([1, 2], [0, 1], [5, 5]),     # repeated new id
+                          ([1, 7], [0, 1], [5, 6]),     # unknown old id
+                          ([1, 1], [0, 1], [5, 6]),     # repeated old id
+                          ([1, 2], [0, 1], [9, 6])):    # new id held by a live sequence
+        with pytest.raises(abi.PagedAttentionError):
+            bm.beam_step(old, par, new)
+        assert (bm.num_free, [bm.refcount(b) for b in range(8)]) == before
+    assert bm.num_tokens(1) == 17 and bm.num_tokens(2) == 17
 
 
 def test_out_of_space_changes_nothing():
