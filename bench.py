@@ -268,9 +268,10 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     if not args.skip_extra:
         extra = run_extra(args, dev, stream)
 
-    serving = None
+    serving = prefix = None
     if not args.skip_serving:
         serving = run_serving(args, dev, stream)
+        prefix = run_prefix_cache(args, dev, stream)
 
     pk = peaks()
     decode_gbs = nb["decode"] / (decode_ms * 1e-3) / 1e9
@@ -315,6 +316,8 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         res["other_decode_workloads"] = extra
     if serving is not None:
         res["serving_loop"] = serving
+    if prefix is not None:
+        res["prefix_cache"] = prefix
     return res
 
 
@@ -340,6 +343,75 @@ def run_extra(args, dev, stream) -> list:
     del w
     out.append(run_cow_step(args, dev, stream))
     return out
+
+
+PREFIX_WORKLOAD = ("prefix_cache_stream_bf16: 512 requests = shared 1000-token system prompt + "
+                   "100-token question, new tokens U[22,356]; budget 2048, chunk 512, <= 256 "
+                   "running; 64/8 heads, d 128; vocab 8192")
+
+
+def run_prefix_cache(args, dev, stream) -> dict:
+    """The prefix-cache scenario of "Inference engine core techniques" 3.3:
+    requests share a 1000-token system prompt and add a 100-token question.
+    The same stream runs through the serving loop with the prefix cache off
+    and on; reported per run: prefill tokens computed, prompt tokens served
+    from the cache, wall time, query tokens/s, and the time to first token
+    (from the stream's start, all requests queued at once)."""
+    import torch
+    from paged_kv_cache_176_gb300.serving import ServingLoop
+
+    vocab = 8192
+    g = np.random.default_rng(args.seed + 11)
+    system = g.integers(0, vocab, size=1000).tolist()
+    reqs = [(system + g.integers(0, vocab, size=100).tolist(), int(g.integers(22, 357)))
+            for _ in range(512)]
+
+    def make(cache):
+        return ServingLoop(65536, 64, 8, 128, dtype=torch.bfloat16, token_budget=2048,
+                           chunk_size=512, max_running=256, max_context=1100 + 356 + 16,
+                           device=dev, seed=args.seed, stream=stream, vocab=vocab,
+                           prefix_cache=cache)
+
+    def run(cache, rq):
+        loop = make(cache)
+        for rid, (p, n) in enumerate(rq):
+            loop.submit(rid, len(p), n, tokens=p)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        evs, toks = [], []
+        t0 = time.perf_counter()
+        while True:
+            p = loop.step()
+            if p is None:
+                break
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            evs.append(ev)
+            toks.append(p.num_tokens)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        assert int(loop.status.item()) == 0
+        st = loop.sched.stats()
+        assert st["finished"] == len(rq)
+        ttft = sorted(e0.elapsed_time(evs[k]) for k in loop.first_token_step.values())
+        res = {"prefix_cache": cache, "steps": len(toks), "wall_s": round(wall, 4),
+               "query_tokens_per_s": round(sum(toks) / wall, 1),
+               "requests_per_s": round(len(rq) / wall, 1),
+               "prefill_tokens": st["prefill_tokens"], "cached_prompt_tokens":
+               loop.sched.cached_tokens, "decode_tokens": st["decode_tokens"],
+               "ttft_ms_mean": round(sum(ttft) / len(ttft), 3),
+               "ttft_ms_p50": round(ttft[len(ttft) // 2], 3)}
+        del loop
+        torch.cuda.empty_cache()
+        return res
+
+    run(True, reqs[:16])  # warm-up
+    off, on = run(False, reqs), run(True, reqs)
+    prompt = sum(len(p) for p, _ in reqs)
+    return {"workload": PREFIX_WORKLOAD, "prompt_tokens": prompt, "cache_off": off, "cache_on": on,
+            "prefill_saved_frac": round(1 - on["prefill_tokens"] / off["prefill_tokens"], 4),
+            "wall_speedup": round(off["wall_s"] / on["wall_s"], 3)}
 
 
 def run_cow_step(args, dev, stream, reps: int = 200) -> dict:
@@ -762,8 +834,12 @@ def main() -> None:
         import torch
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
         torch.cuda.set_device(dev)
-        run = run_mixed if args.only_mixed else run_serving if args.only_serving else run_extra
-        res = run(args, dev, torch.cuda.Stream(dev))
+        st = torch.cuda.Stream(dev)
+        if args.only_serving:
+            res = {"serving_loop": run_serving(args, dev, st),
+                   "prefix_cache": run_prefix_cache(args, dev, st)}
+        else:
+            res = (run_mixed if args.only_mixed else run_extra)(args, dev, st)
     elif args.impl == "reference":
         res = run_reference(args, rank, world)
     else:

@@ -83,6 +83,46 @@ PA_API int pa_bm_append(pa_block_manager* bm, int64_t seq, int n, int64_t* slots
 PA_API int pa_bm_beam_step(pa_block_manager* bm, int n_old, const int64_t* old_ids, int n_new,
                            const int32_t* parents, const int64_t* new_ids);
 
+/*
+ * Prefix cache ("Inference engine core techniques", section 3.2: split the
+ * prompt into pages, hash each page, look the hash up, share the physical
+ * pages that hit by reference count, prefill only the rest). Only full pages
+ * are cached. A page's key is a chain hash: page j of a token sequence hashes
+ * (key of page j-1, its 16 token ids), with key 0 before page 0, so a key
+ * names the whole prefix up to and including the page. The hash is 64-bit
+ * FNV-1a over the 8 little-endian bytes of the previous key and then each
+ * token id as 4 little-endian bytes (pa_page_hash). A lookup also compares
+ * the page's tokens and its parent block, so a hash collision cannot share a
+ * wrong page. A cached block that nobody holds any more stays cached (and
+ * counts as free) until an allocation finds no never-used or uncached free
+ * block and evicts the least recently released one.
+ */
+PA_API uint64_t pa_page_hash(uint64_t parent_key, const int32_t* tokens, int n);
+
+/* Turn the prefix cache on or off (off drops every entry). Default: off. */
+PA_API int pa_bm_set_prefix_cache(pa_block_manager* bm, int enable);
+
+/* Pages currently in the cache (-1 on a NULL manager). */
+PA_API int64_t pa_bm_num_cached(const pa_block_manager* bm);
+
+/*
+ * Register seq, whose first n tokens are tokens[0..n), sharing the longest
+ * run of its leading full pages found in the cache, at most (n-1)/16 pages so
+ * that at least one token is left to compute. *hit_tokens (nullable) receives
+ * the tokens covered (a multiple of 16); the sequence starts with that many
+ * tokens. With the cache off this is pa_bm_add.
+ */
+PA_API int pa_bm_add_cached(pa_block_manager* bm, int64_t seq, const int32_t* tokens, int64_t n,
+                            int64_t* hit_tokens);
+
+/*
+ * Enter seq's full pages among its first n tokens (tokens[0..n), all already
+ * written to the pool) into the cache, after the ones entered before. A page
+ * whose key is already cached (another block with the same prefix) is not
+ * entered twice. n <= pa_bm_num_tokens(seq).
+ */
+PA_API int pa_bm_cache_pages(pa_block_manager* bm, int64_t seq, const int32_t* tokens, int64_t n);
+
 /* Release seq: blocks whose count reaches zero return to the pool. */
 PA_API int pa_bm_free(pa_block_manager* bm, int64_t seq);
 
@@ -106,6 +146,16 @@ PA_API void pa_sched_destroy(pa_scheduler* s);
  * generated tokens (>= 1). PA_EINVAL on a duplicate id or bad lengths. */
 PA_API int pa_sched_submit(pa_scheduler* s, int64_t req_id, int prompt_len, int max_new_tokens);
 
+/* The same with the prompt's token ids (copied). Such a request goes
+ * through the prefix cache when its first prefill chunk is scheduled (not at
+ * admission, so pages written by requests ahead of it in the meantime count):
+ * its cached leading pages are shared and only the rest is prefilled. Its
+ * step tokens appear in the plan's token_ids, its completed pages are entered
+ * into the cache at each commit, and every token it generates must be
+ * supplied to pa_sched_commit_tokens. */
+PA_API int pa_sched_submit_tokens(pa_scheduler* s, int64_t req_id, const int32_t* prompt_tokens,
+                                  int prompt_len, int max_new_tokens);
+
 /* One step's batch, in caller-owned host buffers of the stated capacities.
  * Sequences are ordered decode first (q_len 1), then prefill chunks. The
  * block tables are packed: row j starts at j * table_stride, where
@@ -123,6 +173,8 @@ typedef struct {
   int32_t* cow_src;       /* [max_cow] blocks to copy before the KV write */
   int32_t* cow_dst;       /* [max_cow] */
   int32_t* cow_ntok;      /* [max_cow] filled slots of cow_src to copy (nullable) */
+  int32_t* token_ids;     /* [max_tokens] ids of the step's tokens, -1 for requests
+                             submitted without tokens (nullable) */
 } pa_step_plan;
 
 /* Build the next step (removing finished sequences, admitting requests,
@@ -134,6 +186,15 @@ PA_API int pa_sched_step(pa_scheduler* s, pa_step_plan* plan);
 /* Mark the last planned step as executed: prefill progress advances; a
  * decode step, and the step that finishes a prompt, yield one token. */
 PA_API int pa_sched_commit(pa_scheduler* s);
+
+/* pa_sched_commit for steps with token-mode requests: next_tokens[j] is the
+ * token generated by plan row j (read only for rows that yield one). PA_EINVAL
+ * and nothing changed when next_tokens is NULL and the step holds a token-mode
+ * request. */
+PA_API int pa_sched_commit_tokens(pa_scheduler* s, const int32_t* next_tokens);
+
+/* Prompt tokens admitted from the prefix cache so far (not prefilled). */
+PA_API int64_t pa_sched_cached_tokens(const pa_scheduler* s);
 
 /* Counters: waiting, running, finished requests and the tokens processed. */
 PA_API int pa_sched_stats(const pa_scheduler* s, int64_t* waiting, int64_t* running,

@@ -33,6 +33,7 @@ class _Plan(ctypes.Structure):
         ("context_lens", ctypes.c_void_p), ("block_tables", ctypes.c_void_p),
         ("slot_mapping", ctypes.c_void_p), ("cow_src", ctypes.c_void_p),
         ("cow_dst", ctypes.c_void_p), ("cow_ntok", ctypes.c_void_p),
+        ("token_ids", ctypes.c_void_p),
     ]
 
 
@@ -58,6 +59,22 @@ def _lib() -> ctypes.CDLL:
         lib.pa_bm_append.argtypes = [P, I64, I, P, P, P, P, P]
         lib.pa_bm_beam_step.restype = I
         lib.pa_bm_beam_step.argtypes = [P, I, P, I, P, P]
+        lib.pa_page_hash.restype = ctypes.c_uint64
+        lib.pa_page_hash.argtypes = [ctypes.c_uint64, P, I]
+        lib.pa_bm_set_prefix_cache.restype = I
+        lib.pa_bm_set_prefix_cache.argtypes = [P, I]
+        lib.pa_bm_num_cached.restype = I64
+        lib.pa_bm_num_cached.argtypes = [P]
+        lib.pa_bm_add_cached.restype = I
+        lib.pa_bm_add_cached.argtypes = [P, I64, P, I64, P]
+        lib.pa_bm_cache_pages.restype = I
+        lib.pa_bm_cache_pages.argtypes = [P, I64, P, I64]
+        lib.pa_sched_submit_tokens.restype = I
+        lib.pa_sched_submit_tokens.argtypes = [P, I64, P, I, I]
+        lib.pa_sched_commit_tokens.restype = I
+        lib.pa_sched_commit_tokens.argtypes = [P, P]
+        lib.pa_sched_cached_tokens.restype = I64
+        lib.pa_sched_cached_tokens.argtypes = [P]
         lib.pa_bm_free.restype = I
         lib.pa_bm_free.argtypes = [P, I64]
         lib.pa_bm_num_tokens.restype = I64
@@ -89,6 +106,16 @@ def _lib() -> ctypes.CDLL:
 
 def _np_ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def pa_page_hash(parent_key: int, tokens) -> int:
+    """Chain key of one page (see include/pa_serving.h)."""
+    t = _i32(tokens)
+    return int(_lib().pa_page_hash(parent_key, _np_ptr(t), t.size))
 
 
 class BlockManager:
@@ -159,6 +186,26 @@ class BlockManager:
     def refcount(self, block: int) -> int:
         return int(self._lib.pa_bm_refcount(self._h, block))
 
+    def set_prefix_cache(self, enable: bool) -> None:
+        abi._check("pa_bm_set_prefix_cache", self._lib.pa_bm_set_prefix_cache(self._h, int(enable)))
+
+    @property
+    def num_cached(self) -> int:
+        return int(self._lib.pa_bm_num_cached(self._h))
+
+    def add_cached(self, seq: int, tokens) -> int:
+        """Register seq with prompt ``tokens``; returns the tokens shared from
+        the prefix cache."""
+        t = _i32(tokens)
+        hit = ctypes.c_int64(0)
+        abi._check("pa_bm_add_cached", self._lib.pa_bm_add_cached(self._h, seq, _np_ptr(t), t.size,
+                                                                   ctypes.byref(hit)))
+        return int(hit.value)
+
+    def cache_pages(self, seq: int, tokens) -> None:
+        t = _i32(tokens)
+        abi._check("pa_bm_cache_pages", self._lib.pa_bm_cache_pages(self._h, seq, _np_ptr(t), t.size))
+
 
 class StepPlan:
     """Host buffers of one scheduler step (see pa_step_plan)."""
@@ -172,11 +219,13 @@ class StepPlan:
         self.cow_src = np.zeros(max_cow, dtype=np.int32)
         self.cow_dst = np.zeros(max_cow, dtype=np.int32)
         self.cow_ntok = np.zeros(max_cow, dtype=np.int32)
+        self.token_ids = np.full(max_tokens, -1, dtype=np.int32)
         self.c = _Plan(max_seqs, max_tokens, max_blocks_per_seq, max_cow, 0, 0, 0, 0, 0,
                        _np_ptr(self.seq_ids).value, _np_ptr(self.cu_q_lens).value,
                        _np_ptr(self.context_lens).value, _np_ptr(self.block_tables).value,
                        _np_ptr(self.slot_mapping).value, _np_ptr(self.cow_src).value,
-                       _np_ptr(self.cow_dst).value, _np_ptr(self.cow_ntok).value)
+                       _np_ptr(self.cow_dst).value, _np_ptr(self.cow_ntok).value,
+                       _np_ptr(self.token_ids).value)
 
     @property
     def num_seqs(self) -> int:
@@ -222,16 +271,36 @@ class Scheduler:
             self._lib.pa_sched_destroy(h)
             self._h = None
 
-    def submit(self, req_id: int, prompt_len: int, max_new_tokens: int) -> None:
-        abi._check("pa_sched_submit", self._lib.pa_sched_submit(self._h, req_id, prompt_len,
-                                                                  max_new_tokens))
+    def submit(self, req_id: int, prompt_len: int, max_new_tokens: int, tokens=None) -> None:
+        """Queue a request; with ``tokens`` (the prompt's ids) it goes
+        through the prefix cache and its generated tokens must be committed."""
+        if tokens is None:
+            rc = self._lib.pa_sched_submit(self._h, req_id, prompt_len, max_new_tokens)
+        else:
+            t = _i32(tokens)
+            if t.size != prompt_len:
+                raise ValueError("tokens must hold prompt_len ids")
+            rc = self._lib.pa_sched_submit_tokens(self._h, req_id, _np_ptr(t), prompt_len,
+                                                  max_new_tokens)
+        abi._check("pa_sched_submit", rc)
 
     def step(self, plan: StepPlan) -> StepPlan:
         abi._check("pa_sched_step", self._lib.pa_sched_step(self._h, ctypes.byref(plan.c)))
         return plan
 
-    def commit(self) -> None:
-        abi._check("pa_sched_commit", self._lib.pa_sched_commit(self._h))
+    def commit(self, next_tokens=None) -> None:
+        """Commit the planned step; ``next_tokens[j]`` is the token plan row j
+        generated (needed when the step holds token-mode requests)."""
+        if next_tokens is None:
+            rc = self._lib.pa_sched_commit(self._h)
+        else:
+            t = _i32(next_tokens)
+            rc = self._lib.pa_sched_commit_tokens(self._h, _np_ptr(t))
+        abi._check("pa_sched_commit", rc)
+
+    @property
+    def cached_tokens(self) -> int:
+        return int(self._lib.pa_sched_cached_tokens(self._h))
 
     def stats(self) -> dict:
         v = [ctypes.c_int64(0) for _ in range(5)]
@@ -282,15 +351,27 @@ class ServingLoop:
     With ``fresh_inputs`` the step's q/k/v are redrawn on the device every
     step; otherwise the buffers keep the values drawn at construction (the
     kernels' work does not depend on the values).
+
+    With ``vocab`` the loop runs on token ids: requests carry their prompt's
+    ids, a token's q/k/v are rows of seeded per-token tables (so the same
+    prefix always yields the same cache contents, which is what makes a
+    shared cached page correct), each generated token is a fixed function of
+    the sequence id and position, and ``prefix_cache`` turns on the block
+    manager's prefix cache.
     """
 
     def __init__(self, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                  dtype=torch.bfloat16, token_budget: int = 2048, chunk_size: int = 512,
                  max_running: int = 256, max_context: int = 32768, device="cuda", seed: int = 0,
                  stream: Optional[torch.cuda.Stream] = None, fresh_inputs: bool = True,
-                 max_cow: int = 64):
+                 max_cow: int = 64, vocab: Optional[int] = None, prefix_cache: bool = False):
         self.bm = BlockManager(num_blocks, 16)
+        if prefix_cache:
+            if vocab is None:
+                raise ValueError("the prefix cache needs token ids (vocab)")
+            self.bm.set_prefix_cache(True)
         self.sched = Scheduler(self.bm, token_budget, chunk_size, max_running)
+        self.vocab = vocab
         self.hq, self.hkv, self.d, self.dtype = num_q_heads, num_kv_heads, head_dim, dtype
         self.budget = token_budget
         self.device = torch.device(device)
@@ -308,9 +389,10 @@ class ServingLoop:
         self.v_new = torch.empty_like(self.k_new)
         self.out = torch.empty_like(self.q)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
-        # packed plan: slots (int64) | cu (S+1) | ctx (S) | cow src | dst | ntok | tables
+        # packed plan: slots (int64) | cu (S+1) | ctx (S) | cow src | dst | ntok |
+        # token ids (T) | tables
         self._cap = (_align16(8 * T) + _align16(4 * (S + 1)) + _align16(4 * S) +
-                     3 * _align16(4 * max_cow) + _align16(4 * S * mb))
+                     3 * _align16(4 * max_cow) + _align16(4 * T) + _align16(4 * S * mb))
         self._dev = torch.empty(self._cap, dtype=torch.uint8, device=self.device)
         self._host = [torch.empty(self._cap, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
         self._host_np = [h.numpy() for h in self._host]
@@ -322,16 +404,37 @@ class ServingLoop:
         self.gen = torch.Generator(device=self.device)
         self.gen.manual_seed(seed)
         with torch.cuda.stream(self.stream):
-            self._draw(T)
+            if vocab is None:
+                self._draw(T)
+            else:
+                def table(h):
+                    return torch.randn(vocab, h, head_dim, generator=self.gen, device=self.device,
+                                       dtype=torch.float32).to(dtype)
+                self.emb_q, self.emb_k, self.emb_v = table(num_q_heads), table(num_kv_heads), \
+                    table(num_kv_heads)
         self.scale = head_dim ** -0.5
         self.steps = 0
+        self.prompt_len = {}
+        self.first_token_step = {}  # request id -> step that yielded its first token
 
     def _draw(self, T: int) -> None:
         for t in (self.q[:T], self.k_new[:T], self.v_new[:T]):
             t.copy_(torch.randn(t.shape, generator=self.gen, device=self.device, dtype=torch.float32))
 
-    def submit(self, req_id: int, prompt_len: int, max_new_tokens: int) -> None:
-        self.sched.submit(req_id, prompt_len, max_new_tokens)
+    def submit(self, req_id: int, prompt_len: int, max_new_tokens: int, tokens=None) -> None:
+        if (tokens is None) != (self.vocab is None):
+            raise ValueError("token ids go with a loop built with vocab, and only with it")
+        self.sched.submit(req_id, prompt_len, max_new_tokens, tokens)
+        self.prompt_len[req_id] = prompt_len
+
+    def next_tokens(self, p: StepPlan) -> np.ndarray:
+        """The token each plan row generates: a fixed function of the
+        sequence id and the new token's position (a stand-in sampler)."""
+        S = p.num_seqs
+        x = (p.seq_ids[:S].astype(np.uint64) * np.uint64(0x9E3779B97F4A7C15)
+             + p.context_lens[:S].astype(np.uint64) * np.uint64(0xBF58476D1CE4E5B9))
+        x ^= x >> np.uint64(31)
+        return (x % np.uint64(self.vocab)).astype(np.int32)
 
     def _pack(self, p: StepPlan):
         """Pack the plan into the free pinned buffer; returns the byte offsets."""
@@ -348,6 +451,7 @@ class ServingLoop:
                               ("src", p.cow_src[:C], np.int32),
                               ("dst", p.cow_dst[:C], np.int32),
                               ("ntok", p.cow_ntok[:C], np.int32),
+                              ("ids", p.token_ids[:T] if self.vocab else p.token_ids[:0], np.int32),
                               ("bt", p.block_tables[:S * W], np.int32)):
             n = src.size * np.dtype(dt).itemsize
             buf[o:o + n].view(dt)[:] = src
@@ -370,9 +474,14 @@ class ServingLoop:
             return None
         k, nbytes, offs = self._pack(p)
         with torch.cuda.stream(self.stream):
-            if self.fresh_inputs:
+            if self.vocab is None and self.fresh_inputs:
                 self._draw(T)
             self._dev[:nbytes].copy_(self._host[k][:nbytes], non_blocking=True)
+            if self.vocab is not None:
+                ids = self._view(offs, "ids", torch.int32)
+                torch.index_select(self.emb_q, 0, ids, out=self.q[:T])
+                torch.index_select(self.emb_k, 0, ids, out=self.k_new[:T])
+                torch.index_select(self.emb_v, 0, ids, out=self.v_new[:T])
             ev = torch.cuda.Event()
             ev.record(self.stream)
             self._sent[k] = ev
@@ -395,6 +504,10 @@ class ServingLoop:
                               v_new=self.v_new[:T] if write else None,
                               slot_mapping=slots if write else None,
                               workspace=self.ws, d_status=self.status, stream=self.stream)
-        self.sched.commit()
+        self.sched.commit(self.next_tokens(p) if self.vocab is not None else None)
+        for j in range(p.num_decode, S):  # prefill chunks that finish their prompt
+            sid = int(p.seq_ids[j])
+            if int(p.context_lens[j]) == self.prompt_len.get(sid, -1):
+                self.first_token_step[sid] = self.steps
         self.steps += 1
         return p

@@ -23,6 +23,12 @@ def run_with_oracle(dtype, hq, hkv, d, reqs, num_blocks, budget, chunk, max_runn
                        max_running=max_running, max_context=max_ctx, seed=3)
     for rid, (prompt, new) in enumerate(reqs):
         loop.submit(rid, prompt, new)
+    return drive_with_oracle(loop, num_blocks, len(reqs), dtype)
+
+
+def drive_with_oracle(loop, num_blocks, num_reqs, dtype, on_step=None):
+    """Run the loop to the end, checking every step against the oracle on a
+    host mirror of the pool; ``on_step(plan)`` runs after each check."""
     hk, hv = loop.k_pool.cpu(), loop.v_pool.cpu()  # host mirror of the pool
     mixed_steps = 0
     while True:
@@ -32,8 +38,9 @@ def run_with_oracle(dtype, hq, hkv, d, reqs, num_blocks, budget, chunk, max_runn
         torch.cuda.synchronize()
         S, T = p.num_seqs, p.num_tokens
         for i in range(p.num_cow):
-            hk[int(p.cow_dst[i])] = hk[int(p.cow_src[i])]
-            hv[int(p.cow_dst[i])] = hv[int(p.cow_src[i])]
+            n = int(p.cow_ntok[i])
+            hk[int(p.cow_dst[i]), :n] = hk[int(p.cow_src[i]), :n]
+            hv[int(p.cow_dst[i]), :n] = hv[int(p.cow_src[i]), :n]
         oracle.reshape_and_cache(hk, hv, loop.k_new[:T].cpu(), loop.v_new[:T].cpu(),
                                  torch.from_numpy(p.slot_mapping[:T].copy()))
         ref = oracle.paged_attention(loop.q[:T].cpu(), hk, hv,
@@ -42,12 +49,14 @@ def run_with_oracle(dtype, hq, hkv, d, reqs, num_blocks, budget, chunk, max_runn
                                      torch.from_numpy(p.tables.copy()), loop.scale)
         compare(loop.out[:T], ref, dtype)
         mixed_steps += int(0 < p.num_decode < S)
+        if on_step is not None:
+            on_step(p, hk, hv)
     assert int(loop.status.item()) == 0
     assert np.array_equal(_bytes(loop.k_pool), _bytes(hk))
     assert np.array_equal(_bytes(loop.v_pool), _bytes(hv))
     assert loop.bm.num_free == num_blocks
     st = loop.sched.stats()
-    assert st["finished"] == len(reqs)
+    assert st["finished"] == num_reqs
     return loop.steps, mixed_steps
 
 
@@ -62,6 +71,45 @@ def test_serving_loop_f32_cuda_core_path():
     rng = np.random.default_rng(2)
     reqs = [(int(rng.integers(1, 200)), int(rng.integers(1, 12))) for _ in range(8)]
     run_with_oracle(torch.float32, 8, 2, 64, reqs, 200, 96, 40, 5, 256)
+
+
+@pytest.mark.parametrize("cache", [True, False])
+def test_serving_loop_prefix_cache(cache):
+    # requests share a 100-token system prompt (6 full pages) and add a
+    # question; with the cache on, later requests prefill only what misses
+    rng = np.random.default_rng(4)
+    vocab = 500
+    system = rng.integers(0, vocab, size=100).tolist()
+    reqs = [(system + rng.integers(0, vocab, size=int(rng.integers(1, 60))).tolist(),
+             int(rng.integers(1, 12))) for _ in range(16)]
+    loop = ServingLoop(200, 16, 4, 128, dtype=torch.bfloat16, token_budget=128, chunk_size=64,
+                       max_running=4, max_context=256, seed=5, vocab=vocab, prefix_cache=cache)
+    for rid, (p, n) in enumerate(reqs):
+        loop.submit(rid, len(p), n, tokens=p)
+    toks = {rid: list(p) for rid, (p, _) in enumerate(reqs)}
+    emb_k = loop.emb_k.cpu()
+
+    def check_pages(p, hk, hv):
+        # every sequence's cache holds exactly its tokens' rows, shared or not
+        S = p.num_seqs
+        nxt = loop.next_tokens(p)
+        for j in range(S):
+            sid, ctx = int(p.seq_ids[j]), int(p.context_lens[j])
+            table = p.tables[j]
+            slots = [int(table[q // 16]) * 16 + q % 16 for q in range(ctx)]
+            got = hk.view(-1, 4, 128)[slots]
+            assert torch.equal(got, emb_k[toks[sid][:ctx]]), (sid, ctx)
+            if j < p.num_decode or ctx == len(reqs[sid][0]):
+                toks[sid].append(int(nxt[j]))
+
+    drive_with_oracle(loop, 200, len(reqs), torch.bfloat16, on_step=check_pages)
+    st = loop.sched.stats()
+    prompts = sum(len(p) for p, _ in reqs)
+    if cache:
+        assert loop.sched.cached_tokens >= 96 * 8
+        assert st["prefill_tokens"] == prompts - loop.sched.cached_tokens
+    else:
+        assert loop.sched.cached_tokens == 0 and st["prefill_tokens"] == prompts
 
 
 def test_copy_blocks_bit_exact():
