@@ -80,6 +80,13 @@ struct Cfg {
   static constexpr int kPairs = kC / 2;
   static constexpr int kNt = kTokPerWarp / kTg > 0 ? kTokPerWarp / kTg : 1;
   static constexpr int kBatch = kNt < 4 ? kNt : 4;    // tokens per softmax update per slot
+  // Scores of one batch: kN = kBatch x kGL per lane group of kLpt lanes. When
+  // they split evenly, a reduce-scatter leaves each lane kR complete scores
+  // of one head (kRS); otherwise every lane reduces every score.
+  static constexpr int kN = kBatch * kGL;
+  static constexpr int kR = kLpt >= 2 && kN % kLpt == 0 ? kN / kLpt : 0;
+  static constexpr bool kRS = kR > 0 && kBatch % kR == 0;
+  static constexpr int kLh = kRS ? kBatch / kR : 1;  // lanes holding one head's scores
   static_assert(kC % kVec == 0, "lane slice must be whole 16-byte chunks");
   static_assert(kLanesTok >= 1 && kLanesTok <= 32 && 32 % kLanesTok == 0, "bad lane split");
   static_assert(G % kGL == 0, "bad head split");
@@ -336,6 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   float2 qf[C::kGL][C::kPairs];
   float2 acc[C::kGL][C::kPairs];
   float m[C::kGL], l[C::kGL];
+  float l_own = 0.f;            // reduce-scatter: the sum of this lane's own head
+  const int base = lane - kl;   // first lane of this (token slot, head group)
+  const int own_j = kl * (C::kRS ? C::kR : 0);  // first score this lane owns
+  const int own_h = C::kRS ? own_j / C::kBatch : 0;
+  const int own_b = C::kRS ? own_j % C::kBatch : 0;
   int merges = 0;  // sequences merged across warps so far (mbarrier phase)
 
   int64_t u = 0;
@@ -376,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         }
         m[h] = -INFINITY;
         l[h] = 0.f;
+        l_own = 0.f;
 #pragma unroll
         for (int i = 0; i < C::kPairs; ++i) acc[h][i] = make_float2(0.f, 0.f);
       }
@@ -417,47 +430,118 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 #pragma unroll
           for (int h = 0; h < C::kGL; ++h) sc[b][h] = part[h].x + part[h].y;
         }
-        // complete the dot products across the lanes sharing a (token, head group)
+        if constexpr (C::kRS) {
+          // Reduce-scatter over the kLpt lanes of a (token slot, head group):
+          // scores are laid out head-major (j = h * kBatch + b); each halving
+          // exchange keeps one half, so lane kl ends with the complete scores
+          // j = kl * kR + i, i < kR, all of head own_h.
+          float v[C::kN];
 #pragma unroll
-        for (int off = C::kLpt / 2; off >= 1; off >>= 1)
+          for (int h = 0; h < C::kGL; ++h)
 #pragma unroll
-          for (int b = 0; b < C::kBatch; ++b)
+            for (int b = 0; b < C::kBatch; ++b) v[h * C::kBatch + b] = sc[b][h];
 #pragma unroll
-            for (int h = 0; h < C::kGL; ++h) sc[b][h] += __shfl_xor_sync(0xffffffffu, sc[b][h], off);
-        // online softmax (lazy max, warp-uniform rescale decision)
-        float mx[C::kGL];
-        bool need = false;
+          for (int n = C::kN, off = C::kLpt / 2; off >= 1; n >>= 1, off >>= 1) {
+            const bool upper = (kl & off) != 0;
 #pragma unroll
-        for (int h = 0; h < C::kGL; ++h) {
-          mx[h] = -INFINITY;
+            for (int i = 0; i < n / 2; ++i) {
+              const float send = upper ? v[i] : v[i + n / 2];
+              const float keep = upper ? v[i + n / 2] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+          }
+          // batch max of the lane's head, then of every head on every lane
+          float mo = -INFINITY;
 #pragma unroll
+          for (int i = 0; i < C::kR; ++i) {
+            const int t = sub + WH * (tg + C::kTg * (i0 + own_b + i));
+            if (full || t < ntok) mo = fmaxf(mo, v[i]);
+          }
+#pragma unroll
+          for (int off = 1; off < C::kLh; off <<= 1)
+            mo = fmaxf(mo, __shfl_xor_sync(0xffffffffu, mo, off));
+          float mx[C::kGL];
+          bool need = false;
+#pragma unroll
+          for (int h = 0; h < C::kGL; ++h) {
+            mx[h] = __shfl_sync(0xffffffffu, mo, base + h * C::kLh);
+            need |= mx[h] > m[h] + kRescaleThreshold;
+          }
+          if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int h = 0; h < C::kGL; ++h) {
+              const float mn = mx[h] > m[h] + kRescaleThreshold ? mx[h] : m[h];
+              const float a = merge_factor(m[h], mn);
+              if (own_h == h) l_own *= a;
+#pragma unroll
+              for (int i = 0; i < C::kPairs; ++i)
+                acc[h][i] = make_float2(acc[h][i].x * a, acc[h][i].y * a);
+              m[h] = mn;
+            }
+          }
+          float m_own = m[0];
+#pragma unroll
+          for (int h = 1; h < C::kGL; ++h)
+            if (own_h == h) m_own = m[h];
+          // weights of the lane's own scores, then every lane gathers the
+          // weights of all (token, head) pairs it applies to V
+          float w_own[C::kR];
+#pragma unroll
+          for (int i = 0; i < C::kR; ++i) {
+            const int t = sub + WH * (tg + C::kTg * (i0 + own_b + i));
+            w_own[i] = (full || t < ntok) ? fast_exp2(v[i] - m_own) : 0.f;
+            l_own += w_own[i];
+          }
+#pragma unroll
+          for (int h = 0; h < C::kGL; ++h)
+#pragma unroll
+            for (int b = 0; b < C::kBatch; ++b) {
+              const int j = h * C::kBatch + b;
+              sc[b][h] = __shfl_sync(0xffffffffu, w_own[j % C::kR], base + j / C::kR);
+            }
+        } else {
+          // complete the dot products across the lanes sharing a (token, head group)
+  #pragma unroll
+          for (int off = C::kLpt / 2; off >= 1; off >>= 1)
+  #pragma unroll
+            for (int b = 0; b < C::kBatch; ++b)
+  #pragma unroll
+              for (int h = 0; h < C::kGL; ++h) sc[b][h] += __shfl_xor_sync(0xffffffffu, sc[b][h], off);
+          // online softmax (lazy max, warp-uniform rescale decision)
+          float mx[C::kGL];
+          bool need = false;
+  #pragma unroll
+          for (int h = 0; h < C::kGL; ++h) {
+            mx[h] = -INFINITY;
+  #pragma unroll
+            for (int b = 0; b < C::kBatch; ++b) {
+              const int t = sub + WH * (tg + C::kTg * (i0 + b));
+              if (full || t < ntok) mx[h] = fmaxf(mx[h], sc[b][h]);
+            }
+            need |= mx[h] > m[h] + kRescaleThreshold;
+          }
+          if (__any_sync(0xffffffffu, need)) {
+  #pragma unroll
+            for (int h = 0; h < C::kGL; ++h) {
+              const float mn = mx[h] > m[h] + kRescaleThreshold ? mx[h] : m[h];
+              const float a = merge_factor(m[h], mn);
+              l[h] *= a;
+  #pragma unroll
+              for (int i = 0; i < C::kPairs; ++i)
+                acc[h][i] = make_float2(acc[h][i].x * a, acc[h][i].y * a);
+              m[h] = mn;
+            }
+          }
+  #pragma unroll
           for (int b = 0; b < C::kBatch; ++b) {
             const int t = sub + WH * (tg + C::kTg * (i0 + b));
-            if (full || t < ntok) mx[h] = fmaxf(mx[h], sc[b][h]);
-          }
-          need |= mx[h] > m[h] + kRescaleThreshold;
-        }
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-          for (int h = 0; h < C::kGL; ++h) {
-            const float mn = mx[h] > m[h] + kRescaleThreshold ? mx[h] : m[h];
-            const float a = merge_factor(m[h], mn);
-            l[h] *= a;
-#pragma unroll
-            for (int i = 0; i < C::kPairs; ++i)
-              acc[h][i] = make_float2(acc[h][i].x * a, acc[h][i].y * a);
-            m[h] = mn;
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < C::kBatch; ++b) {
-          const int t = sub + WH * (tg + C::kTg * (i0 + b));
-          const bool valid = full || t < ntok;
-#pragma unroll
-          for (int h = 0; h < C::kGL; ++h) {
-            const float w = valid ? fast_exp2(sc[b][h] - m[h]) : 0.f;
-            sc[b][h] = w;
-            l[h] += w;
+            const bool valid = full || t < ntok;
+  #pragma unroll
+            for (int h = 0; h < C::kGL; ++h) {
+              const float w = valid ? fast_exp2(sc[b][h] - m[h]) : 0.f;
+              sc[b][h] = w;
+              l[h] += w;
+            }
           }
         }
         // P.V
@@ -496,6 +580,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     if (!ok) break;
 
     // ------------------------------------------------------------ finish s
+    // 0. reduce-scatter: each head's sum is split over its kLh lanes
+    if constexpr (C::kRS) {
+#pragma unroll
+      for (int off = 1; off < C::kLh; off <<= 1) l_own += __shfl_xor_sync(0xffffffffu, l_own, off);
+#pragma unroll
+      for (int h = 0; h < C::kGL; ++h) l[h] = __shfl_sync(0xffffffffu, l_own, base + h * C::kLh);
+    }
     // 1. merge the token slots of the warp (lanes with equal head group and kl)
 #pragma unroll
     for (int off = C::kLanesTok; off < 32; off <<= 1) {
