@@ -208,6 +208,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         b.record(stream)
     torch.cuda.synchronize(dev)
     decode_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    gather = gather_ceiling(w, kp, vp, dev, stream)
 
     # timed region: exactly K steps
     dist = world > 1
@@ -304,6 +305,8 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                      "achieved": round(decode_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(decode_gbs / pk["hbm_gbs"], 4), "traffic": traffic,
                      "peak_source": pk["source"], "ms_per_launch": round(decode_ms, 5),
+                     "gather_ceiling": dict(gather, decode_frac_of_ceiling=round(
+                         decode_gbs / gather["gbs"], 4)),
                      "algorithmic_bytes_per_launch": nb["decode"]},
         "e2e": {"value": round(world * nb["step"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
@@ -471,6 +474,35 @@ def run_cow_step(args, dev, stream, reps: int = 200) -> dict:
             "fused_bytes": fused_bytes, "fused_gbs": round(gbs, 1),
             "fused_hbm_frac": round(gbs / pk["hbm_gbs"], 4), "launches_fused": 1,
             "launches_separate": 2}
+
+
+def gather_ceiling(w, kp, vp, dev, stream, stages: int = 3, reps: int = 50) -> dict:
+    """The decode batch's blocks streamed with the decode kernel's copies and
+    stage ring and no compute (include/pa_probe.h): what HBM and the block
+    gather allow on this pool, against which the decode kernel's own time
+    shows how much is spent on the SMs."""
+    import torch
+    import paged_kv_cache_176_gb300 as pa
+
+    ids = [int(w.block_tables[s, j]) for s in range(w.num_seqs)
+           for j in range((int(w.context_lens[s]) + 15) // 16)]
+    blocks = torch.tensor(ids, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(5):
+        pa.abi.pa_gather_probe(kp, vp, blocks, stages=stages, d_status=st, stream=stream)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        pa.abi.pa_gather_probe(kp, vp, blocks, stages=stages, d_status=st, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    assert int(st.item()) == 0
+    us = a.elapsed_time(b) / reps * 1e3
+    nbytes = 2 * len(ids) * kp[0].numel() * kp.element_size()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us": round(us, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+            "frac_of_copy_peak": round(gbs / peaks()["hbm_gbs"], 4), "stages": stages}
 
 
 def run_decode_workload(name: str, w, dev, stream, reps: int = 30, groups=None) -> dict:

@@ -84,6 +84,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_set_decode_ctas.argtypes = [I]
         lib.pa_decode_static_ws.restype = I
         lib.pa_decode_static_ws.argtypes = [PP, P, P, I, I, P, I, P, F, P, P]
+        lib.pa_gather_probe.restype = I
+        lib.pa_gather_probe.argtypes = [PP, P, I, I, I, P, P]
         lib.pa_decode_cascade_workspace_size.restype = SZ
         lib.pa_decode_cascade_workspace_size.argtypes = [I, I, I, I]
         lib.pa_decode_cascade.restype = I
@@ -227,6 +229,19 @@ def pa_decode_cascade(out, q, k_pool, v_pool, block_tables, context_lens, cu_gro
                                  float(scale), _ptr(ws), ws.numel() * ws.element_size(),
                                  _ptr(d_status), _stream(stream)))
     return out
+
+
+def pa_gather_probe(k_pool, v_pool, blocks, stages: int = 3, ctas: int = 0, d_status=None,
+                    stream=None) -> None:
+    """Measurement aid (include/pa_probe.h): stream the listed K/V blocks into
+    shared memory with the decode kernel's copies and compute nothing."""
+    lib = load()
+    pool = make_pool(k_pool, v_pool)
+    if blocks.dtype != torch.int32:
+        raise TypeError("blocks must be int32")
+    _check("pa_gather_probe", lib.pa_gather_probe(ctypes.byref(pool), _ptr(blocks),
+                                                  int(blocks.numel()), stages, ctas,
+                                                  _ptr(d_status), _stream(stream)))
 
 
 PA_DECODE_STATIC_WS_BYTES = 32 << 20

@@ -307,3 +307,21 @@ def test_prefill_tc_chunked_equals_one_pass():
         outs.append(o)
     chunked = torch.cat(outs)
     compare(chunked, ref, torch.bfloat16)
+
+
+def test_gather_probe_runs_and_flags_bad_blocks():
+    # the measurement aid of include/pa_probe.h: no output, only a status
+    k = torch.zeros(64, 16, 8, 128, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    blocks = torch.randperm(64, dtype=torch.int32).cuda()
+    for stages, ctas in ((3, 0), (1, 5), (2, 200)):
+        pa.abi.pa_gather_probe(k, v, blocks, stages=stages, ctas=ctas, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    pa.abi.pa_gather_probe(k, v, torch.tensor([3, 64, 5], dtype=torch.int32, device="cuda"),
+                           d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == pa.abi.PA_STATUS_BAD_BLOCK
+    with pytest.raises(pa.abi.PagedAttentionError):
+        pa.abi.pa_gather_probe(k, v, blocks, stages=4)  # 4 x 64 KB exceeds shared memory
