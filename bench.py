@@ -334,9 +334,12 @@ def run_extra(args, dev, stream) -> list:
     batch through pa_decode and through pa_decode_cascade (one group over the
     62 prefix pages every sequence shares)."""
     from paged_kv_cache_176_gb300 import workloads as W
+    out = [run_decode_workload("tiny_decode_f32: 4 seqs, ctx {17,40,64,100}, 8/2 heads, d 64 "
+                               "(launch-bound)", W.tiny_decode_f32(seed=args.seed), dev, stream,
+                               reps=200)]
     w = W.wide_gqa_decode(seed=args.seed)
-    out = [run_decode_workload("wide_gqa_decode_bf16: 58 seqs x 4096, 16/4 heads, d 256, pool 23305",
-                               w, dev, stream)]
+    out.append(run_decode_workload("wide_gqa_decode_bf16: 58 seqs x 4096, 16/4 heads, d 256, "
+                                   "pool 23305", w, dev, stream))
     w = W.shared_prefix_decode(seed=args.seed)
     out.append(run_decode_workload(SHARED_PREFIX_WORKLOAD, w, dev, stream))
     plen = w.info["shared_pages"] * 16
@@ -611,16 +614,44 @@ def run_mixed(args, dev, stream) -> dict:
     torch.cuda.synchronize(dev)
     one = time.perf_counter() - t0
     n = max(3, min(args.mixed_steps, int(10.0 / max(one, 1e-4))))
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(n):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / n
+    def timed(fn, reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    ms = timed(step, n)
+    # the two slices on their own (each with its own KV write): sequences
+    # 0 .. nd-1 are the decode rows, the rest the prefill chunks
+    cu = w.cu_q_lens.tolist()
+    nd = sum(1 for i in range(w.num_seqs) if cu[i + 1] - cu[i] == 1)
+    S, T = w.num_seqs, w.num_tokens
+
+    def sub(lo, hi):
+        t0, t1 = cu[lo], cu[hi]
+        cu_sub = (d["cu_q_lens"][lo:hi + 1] - t0).contiguous()
+
+        def run():
+            pa.pa_mixed_step(out[t0:t1], d["q"][t0:t1], cu_sub, d["context_lens"][lo:hi],
+                             d["block_tables"][lo:hi], d["k_pool"], d["v_pool"], w.scale,
+                             w.token_budget, k_new=d["k_new"][t0:t1], v_new=d["v_new"][t0:t1],
+                             slot_mapping=d["slot_mapping"][t0:t1], workspace=ws, stream=stream)
+        return run
+
+    for f in (sub(0, nd), sub(nd, S)):
+        for _ in range(3):
+            f()
+    ms_dec = timed(sub(0, nd), n)
+    ms_pf = timed(sub(nd, S), n)
     pk = peaks()
     tflops = work["prefill_flops"] / (ms * 1e-3) / 1e12
+    t_hbm = work["decode_bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3
+    t_tc = work["prefill_flops"] / (pk["bf16_tflops_sustained"] * 1e12) * 1e3
+    pf_tflops = work["prefill_flops"] / (ms_pf * 1e-3) / 1e12
     return {
         "workload": "mixed_step_bf16: budget 2048 = 128 decode (ctx U[1024,8192]) + prefill "
                     "512/512/512/384 at 512-aligned offsets of 32768-token prompts; 64/8 heads, d 128",
@@ -632,6 +663,15 @@ def run_mixed(args, dev, stream) -> dict:
         "decode_gbs_step": round(work["decode_bytes"] / (ms * 1e-3) / 1e9, 1),
         "prefill_flops": work["prefill_flops"],
         "decode_bytes": work["decode_bytes"],
+        "prefill_slice_ms": round(ms_pf, 4),
+        "prefill_slice_tflops": round(pf_tflops, 2),
+        "prefill_slice_tensor_frac": round(pf_tflops / pk["bf16_tflops_sustained"], 4),
+        "decode_slice_ms": round(ms_dec, 4),
+        "decode_slice_gbs": round(work["decode_bytes"] / (ms_dec * 1e-3) / 1e9, 1),
+        "ideal_step_ms": round(max(t_hbm, t_tc), 4),
+        "step_frac": round(max(t_hbm, t_tc) / ms, 4),
+        "note": "ideal_step_ms = max(decode bytes / measured HBM peak, prefill FLOPs / measured "
+                "sustained bf16 peak); slices timed alone, each with its own KV write",
     }
 
 
