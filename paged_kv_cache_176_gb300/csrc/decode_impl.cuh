@@ -35,7 +35,10 @@
 //  * Online softmax in the log2 domain (q pre-scaled by scale*log2 e) with a
 //    lazy running max: the accumulator is rescaled only when a new score
 //    exceeds the running max by more than 8 (weights stay <= 256), decided
-//    per warp so the rescale is a uniform branch.
+//    per warp so the rescale is a uniform branch. The partial dot products of
+//    a batch are reduce-scattered over the lanes of a token group, so each
+//    score's max, weight and sum are computed by one lane only, and the
+//    weights are gathered back for P.V.
 //  * Tokens past the context (the tail of a last block) are never loaded and
 //    never touched, so stale or NaN slots cannot leak into the result.
 #pragma once
