@@ -10,6 +10,7 @@
 
 #include "../../include/pa.h"
 #include "pa_internal.h"
+#include "pa_trace.h"
 
 namespace pa {
 
@@ -121,6 +122,7 @@ int pa_set_decode_ctas(int num_ctas) {
 int pa_reshape_and_cache(const pa_kv_pool* pool, const void* k_new, const void* v_new,
                          const int64_t* slot_mapping, int num_tokens, int* d_status,
                          void* stream) {
+  pa::TraceRange trace("pa_reshape_and_cache");
   int rc = validate_kv_write(pool, k_new, v_new, slot_mapping, num_tokens);
   if (rc != PA_OK || num_tokens == 0) return rc;
   KvWriteArgs a;
@@ -142,6 +144,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
 int pa_decode(const pa_kv_pool* pool, void* out, const void* q, int num_seqs, int num_q_heads,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
               float scale, void* workspace, size_t workspace_bytes, int* d_status, void* stream) {
+  pa::TraceRange trace("pa_decode");
   int rc = check_pool(pool);
   if (rc != PA_OK) return rc;
   if (num_seqs < 0 || max_blocks_per_seq <= 0) return PA_EINVAL;
@@ -200,6 +203,7 @@ int pa_decode_cascade(const pa_kv_pool* pool, void* out, const void* q, int num_
                       const int32_t* context_lens, const int32_t* cu_groups,
                       const int32_t* prefix_lens, int num_groups, float scale, void* workspace,
                       size_t workspace_bytes, int* d_status, void* stream) {
+  pa::TraceRange trace("pa_decode_cascade");
   int rc = check_pool(pool);
   if (rc != PA_OK) return rc;
   if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_groups < 0) return PA_EINVAL;
@@ -282,6 +286,7 @@ int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_
                   int token_budget, const void* k_new, const void* v_new,
                   const int64_t* slot_mapping, void* workspace, size_t workspace_bytes,
                   int* d_status, void* stream) {
+  pa::TraceRange trace("pa_mixed_step");
   int rc = check_pool(pool);
   if (rc != PA_OK) return rc;
   if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq <= 0) return PA_EINVAL;

@@ -26,6 +26,7 @@
 
 #include "../../include/pa.h"
 #include "pa_internal.h"
+#include "pa_trace.h"
 
 namespace pa {
 namespace {
@@ -65,6 +66,7 @@ extern "C" {
 int pa_decode_static_ws(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
                         int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
                         const int32_t* context_lens, float scale, int* d_status, void* stream) {
+  pa::TraceRange trace("pa_decode_static_ws");
   if (pool == nullptr) return PA_EINVAL;
   // the sizes must fit the static scratch; the remaining checks are
   // pa_decode's own

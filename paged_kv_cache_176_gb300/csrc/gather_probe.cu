@@ -4,6 +4,7 @@
 #include "../../include/pa_probe.h"
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "pa_trace.h"
 
 namespace pa {
 namespace {
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(256, 1) gather_probe_kernel(const char* k, con
 
 extern "C" int pa_gather_probe(const pa_kv_pool* pool, const int32_t* blocks, int n, int stages,
                                int ctas, int* d_status, void* stream) {
+  pa::TraceRange trace("pa_gather_probe");
   if (pool == nullptr || pool->k == nullptr || pool->v == nullptr || n < 0) return PA_EINVAL;
   if ((reinterpret_cast<uintptr_t>(pool->k) & 15u) || (reinterpret_cast<uintptr_t>(pool->v) & 15u))
     return PA_EINVAL;

@@ -9,6 +9,7 @@
 #include "../../include/pa_serving.h"
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "pa_trace.h"
 
 namespace pa {
 namespace {
@@ -123,6 +124,7 @@ cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream) {
 
 extern "C" int pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src, const int32_t* dst,
                               int n, int* d_status, void* stream) {
+  pa::TraceRange trace("pa_copy_blocks");
   if (pool == nullptr || pool->k == nullptr || pool->v == nullptr || n < 0) return PA_EINVAL;
   if ((reinterpret_cast<uintptr_t>(pool->k) & 15u) || (reinterpret_cast<uintptr_t>(pool->v) & 15u))
     return PA_EINVAL;
@@ -145,6 +147,7 @@ extern "C" int pa_reshape_and_cache_cow(const pa_kv_pool* pool, const void* k_ne
                                         int num_tokens, const int32_t* cow_src,
                                         const int32_t* cow_dst, const int32_t* cow_ntok,
                                         int n_cow, int* d_status, void* stream) {
+  pa::TraceRange trace("pa_reshape_and_cache_cow");
   if (pool == nullptr || pool->k == nullptr || pool->v == nullptr || num_tokens < 0 || n_cow < 0)
     return PA_EINVAL;
   if ((reinterpret_cast<uintptr_t>(pool->k) & 15u) || (reinterpret_cast<uintptr_t>(pool->v) & 15u))

@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "../../include/pa_serving.h"
+#include "pa_trace.h"
 
 // 64-bit FNV-1a (Fowler, Noll, Vo), fed byte by byte.
 static inline uint64_t fnv1a_byte(uint64_t h, uint8_t b) { return (h ^ b) * 0x100000001b3ull; }
@@ -384,6 +385,7 @@ int pa_sched_submit(pa_scheduler* s, int64_t req_id, int prompt_len, int max_new
 }
 
 int pa_sched_step(pa_scheduler* s, pa_step_plan* plan) {
+  pa::TraceRange trace("pa_sched_step");
   if (s == nullptr || plan == nullptr || s->pending) return PA_EINVAL;
   pa_block_manager* bm = s->bm;
   // 1. finished sequences leave and return their blocks
@@ -494,6 +496,7 @@ int pa_sched_step(pa_scheduler* s, pa_step_plan* plan) {
 }
 
 int pa_sched_commit_tokens(pa_scheduler* s, const int32_t* next_tokens) {
+  pa::TraceRange trace("pa_sched_commit_tokens");
   if (s == nullptr || !s->pending) return PA_EINVAL;
   if (next_tokens == nullptr)
     for (const auto& r : s->running)
