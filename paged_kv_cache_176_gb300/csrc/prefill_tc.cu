@@ -36,11 +36,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "pa_common.cuh"
 #include "pa_internal.h"
 #include "tc_common.cuh"
+#include "tmap.h"
 
 namespace pa {
 namespace {
@@ -541,40 +540,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
 namespace pa {
 namespace {
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled, looked up once through the runtime (no libcuda link).
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// 3-D bf16 tensor {inner, mid, outer} with 128-byte swizzled boxes.
-bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
-               uint32_t box_inner, uint32_t box_mid, uint32_t box_outer) {
-  EncodeTiledFn fn = encode_tiled();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[3] = {inner, mid, outer};
-  const cuuint64_t strides[2] = {inner * 2, inner * mid * 2};  // bytes, dims 1 and 2
-  const cuuint32_t box[3] = {box_inner, box_mid, box_outer};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 bool tc_supported(const PrefillArgs& a) {
   const int group = a.num_q_heads / a.pool.num_kv_heads;
