@@ -42,6 +42,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # decode_reduce_kernel) on the decode batch, from an ncu capture
 # (profiles/decode_b64_bf16.md), valid for the kernel source whose sha256
 # prefix is given; reported as null once the source changes.
+# nominal GB300 figures, reported as a second column beside the measured peaks
+SPEC_HBM_GBS = 7900.0        # HBM3e
+SPEC_BF16_TFLOPS = 2250.0    # dense bf16 tensor
+
 NCU_DECODE_TRAFFIC = {"bytes": 641531392, "src_sha": "4383e146d70f1ce6"}
 
 
@@ -364,6 +368,8 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_kernel + decode_reduce_kernel)",
                      "achieved": round(decode_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(decode_gbs / pk["hbm_gbs"], 4), "traffic": traffic,
+                     "frac_of_spec": round(decode_gbs / SPEC_HBM_GBS, 4),
+                     "spec_peak": SPEC_HBM_GBS,
                      "peak_source": pk["source"], "ms_per_launch": round(decode_ms, 5),
                      "gather_ceiling": dict(gather, decode_frac_of_ceiling=round(
                          decode_gbs / gather["gbs"], 4)),
@@ -732,6 +738,7 @@ def run_mixed(args, dev, stream) -> dict:
         "prefill_slice_ms": round(ms_pf, 4),
         "prefill_slice_tflops": round(pf_tflops, 2),
         "prefill_slice_tensor_frac": round(pf_tflops / pk["bf16_tflops_sustained"], 4),
+        "prefill_slice_frac_of_spec": round(pf_tflops / SPEC_BF16_TFLOPS, 4),
         "decode_slice_ms": round(ms_dec, 4),
         "decode_slice_gbs": round(work["decode_bytes"] / (ms_dec * 1e-3) / 1e9, 1),
         "ideal_step_ms": round(max(t_hbm, t_tc), 4),
