@@ -42,6 +42,18 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # decode_reduce_kernel) on the decode batch, from an ncu capture
 # (profiles/decode_b64_bf16.md), valid for the kernel source whose sha256
 # prefix is given; reported as null once the source changes.
+# The source pages' own figures: other hardware, whole-model serving, none a
+# kernel number for this path; quoted beside the measurements as context only.
+PAGES_CONTEXT = {
+    "serving_tok_s_h100_sxm5_llama33_70b_fp8_128_concurrent": "2,200-2,400 (paged + continuous "
+                                                             "+ chunked); ~1,800 without chunked "
+                                                             "prefill",
+    "decode_tok_s_h100_anchor_model_ctx4096": "~65 at batch 1, ~2,300 at 58 requests (a roofline "
+                                              "bound, not measured)",
+    "paged_attention_kernel_vs_fastertransformer": "20-26 % slower (hardware not stated)",
+    "prefix_cache_ttft_1000_token_shared_prompt": "~50 ms -> ~5 ms (hardware not stated)",
+}
+
 # nominal GB300 figures, reported as a second column beside the measured peaks
 SPEC_HBM_GBS = 7900.0        # HBM3e
 SPEC_BF16_TFLOPS = 2250.0    # dense bf16 tensor
@@ -383,6 +395,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                            "ms_per_step": round(serial_ms, 5),
                            "copies": "the same copies on the compute stream, no overlap"}},
         "gpu_launches": launches_per_step * args.steps,
+        "pages_context": PAGES_CONTEXT,
         "clocks": clk,
     }
     if mixed is not None:
