@@ -257,21 +257,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       S, [&](int s) { return decode_blocks(p, s, &bad_len); }, prefix, warp_sums);
   if (bad_len && blockIdx.x == 0) status_or(p.d_status, PA_STATUS_BAD_LENGTH);
 
-  // Invalid decode sequences (bad lengths) get zero output rows, written once.
-  if (blockIdx.x == 0) {
-    for (int s = warp; s < S; s += kWarps) {
-      bool bad = false;
-      const bool decode_row = decode_blocks(p, s, &bad) > 0 || bad;
-      int q_len = 1;
-      if (p.cu_q_lens != nullptr) q_len = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
-      const int row = query_row(p, s);
-      if (decode_row && bad && q_len == 1 && row >= 0 && row < p.num_rows) {
-        T* o = static_cast<T*>(p.out) + static_cast<int64_t>(row) * p.hq * D;
-        for (int i = lane; i < p.hq * D; i += 32) o[i] = from_float<T>(0.f);
-      }
+  // Invalid decode sequences (bad lengths) get zero output rows, written once:
+  // one warp of the grid checks each sequence, so no CTA lags the others
+  for (int s = blockIdx.x * kWarps + warp; s < S; s += gridDim.x * kWarps) {
+    bool bad = false;
+    const bool decode_row = decode_blocks(p, s, &bad) > 0 || bad;
+    int q_len = 1;
+    if (p.cu_q_lens != nullptr) q_len = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
+    const int row = query_row(p, s);
+    if (decode_row && bad && q_len == 1 && row >= 0 && row < p.num_rows) {
+      T* o = static_cast<T*>(p.out) + static_cast<int64_t>(row) * p.hq * D;
+      for (int i = lane; i < p.hq * D; i += 32) o[i] = from_float<T>(0.f);
     }
-    for (int i = tid; i <= S; i += kThreads) p.ws_prefix[i] = prefix[i];
   }
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= S; i += kThreads) p.ws_prefix[i] = prefix[i];
 
   const int64_t B = prefix[S];
   const int64_t grid = gridDim.x;
