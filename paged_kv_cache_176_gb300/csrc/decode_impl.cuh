@@ -453,27 +453,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
               v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
             }
           }
-          // batch max of the lane's head, then of every head on every lane
-          float mo = -INFINITY;
+          float m_own = m[0];
+#pragma unroll
+          for (int h = 1; h < C::kGL; ++h)
+            if (own_h == h) m_own = m[h];
+          // The running max moves only when a score exceeds it by more than
+          // 8 (rare after a sequence's first batch): each lane tests its own
+          // scores, and only then does the warp find every head's batch max
+          // and rescale, so the common path has no max exchange.
+          bool over = false;
 #pragma unroll
           for (int i = 0; i < C::kR; ++i) {
             const int t = sub + WH * (tg + C::kTg * (i0 + own_b + i));
-            if (full || t < ntok) mo = fmaxf(mo, v[i]);
+            over |= (full || t < ntok) && v[i] > m_own + kRescaleThreshold;
           }
+          if (__any_sync(0xffffffffu, over)) {
+            float mo = -INFINITY;
 #pragma unroll
-          for (int off = 1; off < C::kLh; off <<= 1)
-            mo = fmaxf(mo, __shfl_xor_sync(0xffffffffu, mo, off));
-          float mx[C::kGL];
-          bool need = false;
+            for (int i = 0; i < C::kR; ++i) {
+              const int t = sub + WH * (tg + C::kTg * (i0 + own_b + i));
+              if (full || t < ntok) mo = fmaxf(mo, v[i]);
+            }
 #pragma unroll
-          for (int h = 0; h < C::kGL; ++h) {
-            mx[h] = __shfl_sync(0xffffffffu, mo, base + h * C::kLh);
-            need |= mx[h] > m[h] + kRescaleThreshold;
-          }
-          if (__any_sync(0xffffffffu, need)) {
+            for (int off = 1; off < C::kLh; off <<= 1)
+              mo = fmaxf(mo, __shfl_xor_sync(0xffffffffu, mo, off));
 #pragma unroll
             for (int h = 0; h < C::kGL; ++h) {
-              const float mn = mx[h] > m[h] + kRescaleThreshold ? mx[h] : m[h];
+              const float mx = __shfl_sync(0xffffffffu, mo, base + h * C::kLh);
+              const float mn = mx > m[h] + kRescaleThreshold ? mx : m[h];
               const float a = merge_factor(m[h], mn);
               if (own_h == h) l_own *= a;
 #pragma unroll
@@ -481,11 +488,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
                 acc[h][i] = make_float2(acc[h][i].x * a, acc[h][i].y * a);
               m[h] = mn;
             }
-          }
-          float m_own = m[0];
+            m_own = m[0];
 #pragma unroll
-          for (int h = 1; h < C::kGL; ++h)
-            if (own_h == h) m_own = m[h];
+            for (int h = 1; h < C::kGL; ++h)
+              if (own_h == h) m_own = m[h];
+          }
           // weights of the lane's own scores, then every lane gathers the
           // weights of all (token, head) pairs it applies to V
           float w_own[C::kR];
