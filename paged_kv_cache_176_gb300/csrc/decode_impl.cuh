@@ -417,8 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           float2 part[C::kGL];
 #pragma unroll
           for (int h = 0; h < C::kGL; ++h) part[h] = make_float2(0.f, 0.f);
-          if (full || t < ntok) {
-            const T* krow = kbase + (t * HKV + g) * D;
+          {
+            // loaded whether or not the token is valid (the score of a token
+            // past ntok is never used), so the loads need not wait for ntok;
+            // the row index stays inside the unit
+            const int tl = t < tpu ? t : tpu - 1;
+            const T* krow = kbase + (tl * HKV + g) * D;
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c) {
               float2 kf[C::kVec / 2];
