@@ -90,6 +90,9 @@ struct Cfg {
   static constexpr int kR = kLpt >= 2 && kN % kLpt == 0 ? kN / kLpt : 0;
   static constexpr bool kRS = kR > 0 && kBatch % kR == 0;
   static constexpr int kLh = kRS ? kBatch / kR : 1;  // lanes holding one head's scores
+  // the batch's V words are loaded before the score reduction when they fit
+  // (at most 8 16-byte words per lane); otherwise just before P.V
+  static constexpr bool kPreV = kBatch * kChunks <= 8;
   static_assert(kC % kVec == 0, "lane slice must be whole 16-byte chunks");
   static_assert(kLanesTok >= 1 && kLanesTok <= 32 && 32 % kLanesTok == 0, "bad lane split");
   static_assert(G % kGL == 0, "bad head split");
@@ -200,10 +203,9 @@ __device__ __forceinline__ int query_row(const DecodeParams& p, int s) {
   return p.cu_q_lens != nullptr ? p.cu_q_lens[s] : s;
 }
 
-// 16 bytes of T from shared memory as fp32 pairs.
+// 16 bytes of T as fp32 pairs.
 template <typename T>
-__device__ __forceinline__ void load_pairs(const T* src, float2* dst) {
-  const uint4 raw = *reinterpret_cast<const uint4*>(src);
+__device__ __forceinline__ void unpack_pairs(const uint4 raw, float2* dst) {
   if constexpr (sizeof(T) == 2) {
     dst[0] = bf16x2_to_float2(raw.x);
     dst[1] = bf16x2_to_float2(raw.y);
@@ -213,6 +215,12 @@ __device__ __forceinline__ void load_pairs(const T* src, float2* dst) {
     dst[0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
     dst[1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
   }
+}
+
+// 16 bytes of T from shared memory as fp32 pairs.
+template <typename T>
+__device__ __forceinline__ void load_pairs(const T* src, float2* dst) {
+  unpack_pairs<T>(*reinterpret_cast<const uint4*>(src), dst);
 }
 
 // Rescale factor of a partial with running max m when the merged max is mn.
@@ -437,6 +445,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 #pragma unroll
           for (int h = 0; h < C::kGL; ++h) sc[b][h] = part[h].x + part[h].y;
         }
+        // the batch's V words, loaded now (row index clamped into the unit;
+        // the P.V of a token past ntok is skipped) so that their latency
+        // overlaps the score reduction
+        uint4 vraw[C::kPreV ? C::kBatch : 1][C::kPreV ? C::kChunks : 1];
+        if constexpr (C::kPreV) {
+#pragma unroll
+          for (int b = 0; b < C::kBatch; ++b) {
+            const int t = sub + WH * (tg + C::kTg * (i0 + b));
+            const int tl = t < tpu ? t : tpu - 1;
+            const T* vrow = vbase + (tl * HKV + g) * D;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+              vraw[b][c] = *reinterpret_cast<const uint4*>(vrow + (kl + C::kLpt * c) * C::kVec);
+          }
+        }
         if constexpr (C::kRS) {
           // Reduce-scatter over the kLpt lanes of a (token slot, head group):
           // scores are laid out head-major (j = h * kBatch + b); each halving
@@ -563,11 +586,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         for (int b = 0; b < C::kBatch; ++b) {
           const int t = sub + WH * (tg + C::kTg * (i0 + b));
           if (full || t < ntok) {
-            const T* vrow = vbase + (t * HKV + g) * D;
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c) {
               float2 vf[C::kVec / 2];
-              load_pairs(vrow + (kl + C::kLpt * c) * C::kVec, vf);
+              if constexpr (C::kPreV) {
+                unpack_pairs<T>(vraw[b][c], vf);
+              } else {
+                load_pairs(vbase + (t * HKV + g) * D + (kl + C::kLpt * c) * C::kVec, vf);
+              }
 #pragma unroll
               for (int h = 0; h < C::kGL; ++h) {
                 const float2 w2 = make_float2(sc[b][h], sc[b][h]);
