@@ -305,10 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   constexpr int kTokenBytes = HKV * D * C::kElt;
 
   // Issue unit u into its stage (called by one lane).
-  auto issue = [&](int64_t u) {
-    const int st = static_cast<int>(u % L.stages);
-    const int64_t rel = u / parts;  // block of the CTA's range
-    const int part = static_cast<int>(u % parts);
+  // Issue unit u into stage st (= u % stages; the caller keeps it).
+  auto issue = [&](int u, int st) {
+    const int rel = parts == 1 ? u : u / parts;  // block of the CTA's range
+    const int part = parts == 1 ? 0 : u % parts;
     int phys, block_tokens;
     if (rel < kTableCache) {
       phys = table[rel];
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     }
   };
   if (tid == 0) {
-    for (int64_t u = 0; u < min(static_cast<int64_t>(L.stages), n_units); ++u) issue(u);
+    for (int u = 0; u < min(static_cast<int64_t>(L.stages), n_units); ++u) issue(u, u);
   }
 
   // ---------------------------------------------------------------- consumers
@@ -361,11 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   const int own_b = C::kRS ? own_j % C::kBatch : 0;
   int merges = 0;  // sequences merged across warps so far (mbarrier phase)
 
-  int64_t u = 0;
+  int u = 0;
+  int st_c = 0;       // stage of unit u (u % stages) and its mbarrier phase,
+  uint32_t ph_c = 0;  // kept incrementally: no division per unit
   int s = upper_index(prefix, S, lo);
   bool ok = true;
   while (u < n_units && ok) {
-    while (prefix[s + 1] <= lo + u / parts) ++s;
+    while (prefix[s + 1] <= lo + (parts == 1 ? u : u / parts)) ++s;
     const int64_t seq_lo = max(lo, static_cast<int64_t>(prefix[s]));
     const int64_t seq_hi = min(hi, static_cast<int64_t>(prefix[s + 1]));
     const int64_t seq_units = (seq_hi - seq_lo) * parts;
@@ -406,9 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     }
     bool poisoned = false;
 
-    for (int64_t su = 0; su < seq_units; ++su, ++u) {
-      const int st = static_cast<int>(u % L.stages);
-      const uint32_t parity = static_cast<uint32_t>((u / L.stages) & 1);
+    for (int su = 0; su < seq_units; ++su, ++u) {
+      const int st = st_c;
+      const uint32_t parity = ph_c;
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], parity));
       if (!ok) break;
       const int ntok = flags[st];
@@ -613,8 +615,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         if (prev == kWarps - 1) {
           done[st] = 0;
           __threadfence_block();
-          if (u + L.stages < n_units) issue(u + L.stages);
+          if (u + L.stages < n_units) issue(u + L.stages, st);
         }
+      }
+      if (++st_c == L.stages) {
+        st_c = 0;
+        ph_c ^= 1;
       }
     }
     if (!ok) break;
