@@ -828,6 +828,8 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
   bool poisoned = false;
+  // with at least as many blocks as CTAs no CTA range is empty: skip the test
+  const bool all_nonempty = B >= grid;
   for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
     float2 ml[4];
     float v[4][kPer];
@@ -835,7 +837,7 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int64_t c = c0 + j;
-      use[j] = c <= c_last && (c * B / grid != (c + 1) * B / grid);
+      use[j] = c <= c_last && (all_nonempty || c * B / grid != (c + 1) * B / grid);
       if (use[j]) {
         ml[j] = p.ws_ml[(c + s) * p.hq + h];
         const float* src = p.ws_acc + ((c + s) * p.hq + h) * D + lane * kPer;
