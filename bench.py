@@ -58,7 +58,7 @@ PAGES_CONTEXT = {
 SPEC_HBM_GBS = 7900.0        # HBM3e
 SPEC_BF16_TFLOPS = 2250.0    # dense bf16 tensor
 
-NCU_DECODE_TRAFFIC = {"bytes": 641549824, "src_sha": "0201a194b050869b"}
+NCU_DECODE_TRAFFIC = {"bytes": 641277440, "src_sha": "6d80203b4d46e49f"}
 
 
 def _src_sha(path: str) -> str:
