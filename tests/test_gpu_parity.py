@@ -99,6 +99,22 @@ def test_decode_split_counts(ctas):
     assert int(db.status.item()) == 0
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_cta_range_beyond_table_cache(dtype):
+    """One CTA owning more blocks than it stages in shared memory (1,063 >
+    1,024): the refills past the staged table read the block table directly;
+    fp32 with 8 KV heads moves half blocks (two units per block)."""
+    w = W.paged_workload("long", 13, [9000, 8000], [1, 1], 32, 8, 128, 1300, dtype,
+                         write_new=True)
+    pa.pa_set_decode_ctas(1)
+    try:
+        out, db = run_decode(w)
+    finally:
+        pa.pa_set_decode_ctas(0)
+    compare(out, oracle_out(w), dtype)
+    assert int(db.status.item()) == 0
+
+
 @pytest.mark.parametrize("d,hq,hkv,dtype", [
     (64, 8, 8, torch.bfloat16), (64, 16, 2, torch.float32), (128, 8, 1, torch.bfloat16),
     (128, 16, 4, torch.float32), (256, 16, 8, torch.bfloat16), (256, 8, 1, torch.float32),
