@@ -287,30 +287,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   const int64_t hi = (static_cast<int64_t>(blockIdx.x) + 1) * B / grid;
   if (lo >= hi) return;
 
-  // stage this CTA's slice of the block tables (first kTableCache blocks)
-  // with the number of context tokens each block holds
-  const int n_cached = static_cast<int>(min(hi - lo, static_cast<int64_t>(kTableCache)));
-  for (int i = tid; i < n_cached; i += kThreads) {
-    const int s = upper_index(prefix, S, lo + i);
-    bool unused = false;
-    const int j = static_cast<int>(lo + i - prefix[s]) + prefix_blocks(p, s, p.context_lens[s], &unused);
-    table[i] = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
-    block_ntok[i] = static_cast<uint8_t>(min(kBlockSize, p.context_lens[s] - j * kBlockSize));
-  }
-  __syncthreads();
-
   const int parts = L.parts;
   const int tpu = L.tokens_per_unit;
   const int64_t n_units = (hi - lo) * parts;
   constexpr int kTokenBytes = HKV * D * C::kElt;
 
-  // Issue unit u into its stage (called by one lane).
-  // Issue unit u into stage st (= u % stages; the caller keeps it).
-  auto issue = [&](int u, int st) {
+  // Issue unit u into stage st (= u % stages; the caller keeps it), called
+  // by one lane; `direct` reads the block table in global memory instead of
+  // the staged slice.
+  auto issue = [&](int u, int st, bool direct) {
     const int rel = parts == 1 ? u : u / parts;  // block of the CTA's range
     const int part = parts == 1 ? 0 : u % parts;
     int phys, block_tokens;
-    if (rel < kTableCache) {
+    if (rel < kTableCache && !direct) {
       phys = table[rel];
       block_tokens = block_ntok[rel];
     } else {
@@ -339,9 +328,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       bulk_g2s(kdst + L.part_bytes, p.v_pool + src, bytes, &bars[st]);
     }
   };
+  // the first stages are issued from the global table at once, so their
+  // copies are in flight while the CTA stages the rest of its table slice
   if (tid == 0) {
-    for (int u = 0; u < min(static_cast<int64_t>(L.stages), n_units); ++u) issue(u, u);
+    for (int u = 0; u < min(static_cast<int64_t>(L.stages), n_units); ++u) issue(u, u, true);
   }
+
+
+  // stage this CTA's slice of the block tables (first kTableCache blocks)
+  // with the number of context tokens each block holds
+  const int n_cached = static_cast<int>(min(hi - lo, static_cast<int64_t>(kTableCache)));
+  for (int i = tid; i < n_cached; i += kThreads) {
+    const int s = upper_index(prefix, S, lo + i);
+    bool unused = false;
+    const int j = static_cast<int>(lo + i - prefix[s]) + prefix_blocks(p, s, p.context_lens[s], &unused);
+    table[i] = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
+    block_ntok[i] = static_cast<uint8_t>(min(kBlockSize, p.context_lens[s] - j * kBlockSize));
+  }
+  __syncthreads();
 
   // ---------------------------------------------------------------- consumers
   const int g = warp % HKV;     // this warp's KV head
@@ -615,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         if (prev == kWarps - 1) {
           done[st] = 0;
           __threadfence_block();
-          if (u + L.stages < n_units) issue(u + L.stages, st);
+          if (u + L.stages < n_units) issue(u + L.stages, st, false);
         }
       }
       if (++st_c == L.stages) {
