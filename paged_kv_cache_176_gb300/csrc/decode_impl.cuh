@@ -346,6 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     block_ntok[i] = static_cast<uint8_t>(min(kBlockSize, p.context_lens[s] - j * kBlockSize));
   }
   __syncthreads();
+  // the merge kernel may be launched now: it waits (griddepcontrol.wait) for
+  // this whole grid to complete before it reads anything
+  pdl_launch_dependents();
 
   // ---------------------------------------------------------------- consumers
   const int g = warp % HKV;     // this warp's KV head
@@ -790,7 +793,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     }
   }
   if (!ok && lane == 0) status_or(p.d_status, PA_STATUS_TIMEOUT);
-  pdl_launch_dependents();
 }
 
 // Merge the partials of sequences that straddle CTAs: o = sum_c a_c acc_c /
