@@ -61,6 +61,32 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// ldmatrix: four 8 x 8 bf16 matrices; lanes 8i .. 8i+7 give the row
+// addresses of matrix i, and lane t receives row t/4, columns 2(t%4), 2(t%4)+1
+// of each (the transposed pair with .trans).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// c (16 x 8, fp32) += a (16 x 16, bf16, row-major) * b (16 x 8, bf16, column-major)
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 template <typename T, int D, int G, int WH>
 struct Cfg {
   static constexpr int kHkv = kWarps / WH;
@@ -93,6 +119,11 @@ struct Cfg {
   // the batch's V words are loaded before the score reduction when they fit
   // (at most 8 16-byte words per lane); otherwise just before P.V
   static constexpr bool kPreV = kBatch * kChunks <= 8;
+  // bf16 with head_dim 64 or 128 and one warp per KV head runs the products
+  // on the tensor cores (mma.sync m16n8k16, fp32 accumulate): the group's
+  // query heads are the rows of a 16-row tile, the block's 16 tokens its
+  // columns (Q K^T) or its reduction dimension (P V).
+  static constexpr bool kMma = sizeof(T) == 2 && (D == 64 || D == 128) && WH == 1 && G <= 16;
   static_assert(kC % kVec == 0, "lane slice must be whole 16-byte chunks");
   static_assert(kLanesTok >= 1 && kLanesTok <= 32 && 32 % kLanesTok == 0, "bad lane split");
   static_assert(G % kGL == 0, "bad head split");
@@ -102,19 +133,21 @@ struct SmemLayout {
   int stages;
   int tokens_per_unit;  // tokens of one block moved per pipeline stage (16, 8 or 4)
   int parts;            // 16 / tokens_per_unit
-  int part_bytes;       // one K (or V) part: tokens_per_unit * Hkv * D * elt
+  int pair_pitch;       // bytes from one pair of token rows (all KV heads) to the next
+  int part_bytes;       // one K (or V) part: tokens_per_unit / 2 * pair_pitch
   int off_bars, off_done, off_flags, off_mbars, off_table, off_ntok, off_merge, off_prefix, total;
 };
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline SmemLayout make_layout(int stages, int tokens_per_unit, int hkv, int d,
-                                                  int elt, int wh, int group, int num_seqs) {
+                                                  int elt, int wh, int group, int num_seqs, int pair_pad) {
   SmemLayout L;
   L.stages = stages;
   L.tokens_per_unit = tokens_per_unit;
   L.parts = kBlockSize / tokens_per_unit;
-  L.part_bytes = tokens_per_unit * hkv * d * elt;
+  L.pair_pitch = 2 * hkv * d * elt + pair_pad;
+  L.part_bytes = tokens_per_unit / 2 * L.pair_pitch;
   const int off = stages * 2 * L.part_bytes;
   L.off_bars = align_up(off, 16);
   L.off_done = L.off_bars + stages * 8;
@@ -324,8 +357,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       const int64_t src = (static_cast<int64_t>(phys) * kBlockSize + part * tpu) * kTokenBytes;
       char* kdst = smem + st * 2 * L.part_bytes;
       mbar_arrive_expect_tx(&bars[st], 2 * bytes);
-      bulk_g2s(kdst, p.k_pool + src, bytes, &bars[st]);
-      bulk_g2s(kdst + L.part_bytes, p.v_pool + src, bytes, &bars[st]);
+      if constexpr (C::kMma) {
+        for (int t = 0; t < ntok; t += 2) {
+          const uint32_t b2 = static_cast<uint32_t>(min(2, ntok - t) * kTokenBytes);
+          bulk_g2s(kdst + (t / 2) * L.pair_pitch, p.k_pool + src + t * kTokenBytes, b2, &bars[st]);
+          bulk_g2s(kdst + L.part_bytes + (t / 2) * L.pair_pitch, p.v_pool + src + t * kTokenBytes, b2,
+                   &bars[st]);
+        }
+      } else {
+        bulk_g2s(kdst, p.k_pool + src, bytes, &bars[st]);
+        bulk_g2s(kdst + L.part_bytes, p.v_pool + src, bytes, &bars[st]);
+      }
     }
   };
   // the first stages are issued from the global table at once, so their
@@ -349,6 +391,218 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   // the merge kernel may be launched now: it waits (griddepcontrol.wait) for
   // this whole grid to complete before it reads anything
   pdl_launch_dependents();
+
+  if constexpr (C::kMma) {
+    // -------------------------------------------------- tensor-core consumers
+    // Warp g serves KV head g. Per block: S (16 rows x 16 tokens) = Q K^T in
+    // D / 16 k-steps, each two m16n8k16 MMAs; the online softmax runs on the
+    // S fragments in fp32; O (16 rows x D) += P V with P re-packed from the S
+    // fragments as the A operand. Rows are the group's query heads (G of 16
+    // are real), so lane t owns rows t/4 and t/4 + 8, columns 2(t%4), +1.
+    // Column n of S n-tile j is token 2n + j (the even tokens, then the odd
+    // ones), which keeps every ldmatrix conflict-free on the padded layout;
+    // P V takes its k index in the same order.
+    const int g = warp;
+    const int gi = lane >> 2, qi = lane & 3;
+    constexpr int KS = D / 16;
+    // ldmatrix row addresses of this lane inside a K / V part (token t sits
+    // at (t / 2) pairs + (t % 2) rows): K matrices are (even | odd tokens) x
+    // (d lo | hi) of a k-step, V (.trans) matrices are (even | odd tokens) x
+    // (d of n-tile 2n | 2n+1)
+    const int lm = lane >> 3, lr = lane & 7;
+    const uint32_t k_lane = static_cast<uint32_t>(lr * L.pair_pitch + (lm >> 1) * kTokenBytes +
+                                                  (g * D + (lm & 1) * 8) * 2);
+    const uint32_t v_lane = static_cast<uint32_t>(lr * L.pair_pitch + (lm & 1) * kTokenBytes +
+                                                  (g * D + (lm >> 1) * 8) * 2);
+    const uint32_t sbase = smem_addr(smem);
+    uint32_t qa[KS][4];
+    float o[D / 8][4];
+    int u = 0;
+    int st_c = 0;
+    uint32_t ph_c = 0;
+    int s = upper_index(prefix, S, lo);
+    bool ok = true;
+    while (u < n_units && ok) {
+      while (prefix[s + 1] <= lo + (parts == 1 ? u : u / parts)) ++s;
+      const int64_t seq_lo = max(lo, static_cast<int64_t>(prefix[s]));
+      const int64_t seq_hi = min(hi, static_cast<int64_t>(prefix[s + 1]));
+      const int64_t seq_units = (seq_hi - seq_lo) * parts;
+      const bool whole = prefix[s] >= lo && prefix[s + 1] <= hi;
+      const int row = query_row(p, s);
+      bool pre_bad = false;
+      const bool has_pre = prefix_blocks(p, s, p.context_lens[s], &pre_bad) > 0;
+      // Q as stored (bf16 pairs); the scale is applied to the fp32 scores
+      {
+        const uint32_t* q = reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) +
+                                                              static_cast<int64_t>(row) * p.hq * D);
+        const int h0 = g * G + gi, h1 = g * G + gi + 8;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const int c = (16 * kk + 2 * qi) / 2;  // bf16-pair index
+          qa[kk][0] = gi < G ? __ldg(q + h0 * (D / 2) + c) : 0u;
+          qa[kk][1] = gi + 8 < G ? __ldg(q + h1 * (D / 2) + c) : 0u;
+          qa[kk][2] = gi < G ? __ldg(q + h0 * (D / 2) + c + 4) : 0u;
+          qa[kk][3] = gi + 8 < G ? __ldg(q + h1 * (D / 2) + c + 4) : 0u;
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      bool poisoned = false;
+
+      for (int su = 0; su < seq_units; ++su, ++u) {
+        const int st = st_c;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], ph_c));
+        if (!ok) break;
+        const int ntok = flags[st];
+        if (ntok < 0) poisoned = true;
+        if (ntok > 0) {
+          const uint32_t kb = sbase + static_cast<uint32_t>(st * 2 * L.part_bytes);
+          const uint32_t vb = kb + static_cast<uint32_t>(L.part_bytes);
+          if (ntok < kBlockSize) {
+            // rows past the context were not copied and may hold anything:
+            // zero this head's slice of the value rows (their weight is 0)
+            char* vrow = smem + st * 2 * L.part_bytes + L.part_bytes + g * D * 2;
+            constexpr int kChunkRow = D * 2 / 16;
+            for (int i = lane; i < (kBlockSize - ntok) * kChunkRow; i += 32) {
+              const int t = ntok + i / kChunkRow;
+              *reinterpret_cast<uint4*>(vrow + (t / 2) * L.pair_pitch + (t % 2) * kTokenBytes +
+                                        (i % kChunkRow) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // ordered before the stage's next bulk copy
+            __syncwarp();
+          }
+          float sc[2][4];
+#pragma unroll
+          for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            uint32_t kf[4];
+            ldsm_x4(kb + k_lane + kk * 32, kf);
+            mma_16816(sc[0], qa[kk], kf[0], kf[1]);
+            mma_16816(sc[1], qa[kk], kf[2], kf[3]);
+          }
+          // log2-domain scores; tokens past the context are masked
+          float mt0 = -INFINITY, mt1 = -INFINITY;
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const bool valid = 2 * (2 * qi + e) + n < ntok;  // token of column 2qi+e of n-tile n
+              sc[n][e] = valid ? sc[n][e] * p.scale_log2 : -INFINITY;
+              sc[n][2 + e] = valid ? sc[n][2 + e] * p.scale_log2 : -INFINITY;
+              mt0 = fmaxf(mt0, sc[n][e]);
+              mt1 = fmaxf(mt1, sc[n][2 + e]);
+            }
+#pragma unroll
+          for (int off = 1; off <= 2; off <<= 1) {
+            mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, off));
+            mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, off));
+          }
+          // lazy running max: moved only when a score exceeds it by more than 8
+          const bool need0 = mt0 > m0 + kRescaleThreshold, need1 = mt1 > m1 + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need0 || need1)) {
+            const float n0 = need0 ? mt0 : m0, n1 = need1 ? mt1 : m1;
+            const float a0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - n0);
+            const float a1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - n1);
+            l0 *= a0;
+            l1 *= a1;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+              o[n][0] *= a0;
+              o[n][1] *= a0;
+              o[n][2] *= a1;
+              o[n][3] *= a1;
+            }
+            m0 = n0;
+            m1 = n1;
+          }
+          float w[2][4];
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            w[n][0] = fast_exp2(sc[n][0] - m0);
+            w[n][1] = fast_exp2(sc[n][1] - m0);
+            w[n][2] = fast_exp2(sc[n][2] - m1);
+            w[n][3] = fast_exp2(sc[n][3] - m1);
+          }
+          l0 += (w[0][0] + w[0][1]) + (w[1][0] + w[1][1]);
+          l1 += (w[0][2] + w[0][3]) + (w[1][2] + w[1][3]);
+          const uint32_t pa[4] = {pack_bf16x2(w[0][0], w[0][1]), pack_bf16x2(w[0][2], w[0][3]),
+                                  pack_bf16x2(w[1][0], w[1][1]), pack_bf16x2(w[1][2], w[1][3])};
+#pragma unroll
+          for (int np = 0; np < KS; ++np) {
+            uint32_t vf[4];
+            ldsm_x4_trans(vb + v_lane + np * 32, vf);
+            mma_16816(o[2 * np], pa, vf[0], vf[1]);
+            mma_16816(o[2 * np + 1], pa, vf[2], vf[3]);
+          }
+        }
+        // stage consumed by this warp; the last warp to finish refills it
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          const int prev = atomicAdd(&done[st], 1);
+          if (prev == kWarps - 1) {
+            done[st] = 0;
+            __threadfence_block();
+            if (u + L.stages < n_units) issue(u + L.stages, st, false);
+          }
+        }
+        if (++st_c == L.stages) {
+          st_c = 0;
+          ph_c ^= 1;
+        }
+      }
+      if (!ok) break;
+
+      // ------------------------------------------------------------ finish s
+#pragma unroll
+      for (int off = 1; off <= 2; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int hr = gi + 8 * r;  // row of the tile = query head of the group
+        if (hr >= G) continue;
+        const int head = g * G + hr;
+        float mr = r ? m1 : m0, lr_ = r ? l1 : l0;
+        if (whole) {
+          bool pre_poisoned = false;
+          if (has_pre) {
+            // fold in the shared-prefix partial of this sequence
+            const int64_t idx = static_cast<int64_t>(s) * p.hq + head;
+            const float2 pml = p.pre_ml[idx];
+            pre_poisoned = pml.y < 0.f;
+            const float mn = fmaxf(mr, pml.x);
+            const float a = merge_factor(mr, mn), b = merge_factor(pml.x, mn);
+            lr_ = lr_ * a + pml.y * b;
+            const float* prow = p.pre_acc + idx * D;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+              const float2 pv = *reinterpret_cast<const float2*>(prow + 8 * n + 2 * qi);
+              o[n][2 * r] = o[n][2 * r] * a + pv.x * b;
+              o[n][2 * r + 1] = o[n][2 * r + 1] * a + pv.y * b;
+            }
+          }
+          const float inv = (poisoned || pre_poisoned) ? 0.f : 1.f / lr_;
+          uint32_t* orow = reinterpret_cast<uint32_t*>(static_cast<T*>(p.out) +
+                                                       (static_cast<int64_t>(row) * p.hq + head) * D);
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n) orow[4 * n + qi] = pack_bf16x2(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
+        } else {
+          const int64_t slot = static_cast<int64_t>(blockIdx.x) + s;
+          if (qi == 0) p.ws_ml[slot * p.hq + head] = make_float2(mr, poisoned ? -1.f : lr_);
+          float* arow = p.ws_acc + (slot * p.hq + head) * D;
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n)
+            *reinterpret_cast<float2*>(arow + 8 * n + 2 * qi) = make_float2(o[n][2 * r], o[n][2 * r + 1]);
+        }
+      }
+    }
+    if (!ok && lane == 0) status_or(p.d_status, PA_STATUS_TIMEOUT);
+    return;
+  }
 
   // ---------------------------------------------------------------- consumers
   const int g = warp % HKV;     // this warp's KV head
@@ -893,9 +1147,12 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   int tpu = kBlockSize;
   while (tpu > 4 && 2 * tpu * token_bytes > 64 * 1024) tpu /= 2;
   const int smem_limit = 227 * 1024 - 1024;  // leave room for static shared memory
-  SmemLayout L = make_layout(4, tpu, hkv, D, elt, WH, G, a.num_seqs);
-  if (L.total > smem_limit) L = make_layout(3, tpu, hkv, D, elt, WH, G, a.num_seqs);
-  if (L.total > smem_limit) L = make_layout(2, tpu, hkv, D, elt, WH, G, a.num_seqs);
+  // the tensor-core path pads every pair of token rows by 16 bytes, so the
+  // even (or the odd) tokens of one KV head fall in different banks
+  const int pad = Cfg<T, D, G, WH>::kMma ? 16 : 0;
+  SmemLayout L = make_layout(4, tpu, hkv, D, elt, WH, G, a.num_seqs, pad);
+  if (L.total > smem_limit) L = make_layout(3, tpu, hkv, D, elt, WH, G, a.num_seqs, pad);
+  if (L.total > smem_limit) L = make_layout(2, tpu, hkv, D, elt, WH, G, a.num_seqs, pad);
   if (L.total > smem_limit) return cudaErrorInvalidValue;
 
   int grid = a.grid_override > 0 ? a.grid_override : device_sm_count();
