@@ -1,4 +1,4 @@
-// decode_impl.cuh -- paged decode attention on sm_103a (SIMT, HBM-bound).
+// decode_impl.cuh -- paged decode attention on sm_103a (HBM-bound).
 // Included by one translation unit per (dtype, head_dim): decode_<dtype>_d<D>.cu.
 //
 // What it computes: for every decode sequence s and query head h (KV head
@@ -20,27 +20,38 @@
 //    any relabelling of physical blocks or sharing of blocks.
 //  * A pool block stores its 16 tokens x all KV heads contiguously, so one
 //    1-D bulk copy (cp.async.bulk) moves a whole block of K (and one of V)
-//    into shared memory: 16-byte aligned, fully coalesced. A 3-4 stage
+//    into shared memory: 16-byte aligned, fully coalesced (four copies of 4
+//    token rows each on the tensor-core path below). A 3-4 stage
 //    mbarrier pipeline keeps >= 2 blocks (up to 128 KB) in flight per SM. The
 //    CTA's slice of the block tables is staged in shared memory up front.
 //  * Warps are decoupled: each waits only on the stage it reads, and the last
 //    warp to finish a stage (a shared-memory counter) refills it. No CTA-wide
 //    barrier runs in the steady state.
-//  * Warp w serves KV head w % Hkv (and 1/WH of each block's tokens when a
-//    KV head has WH > 1 warps). Up to four query heads of the GQA group live
-//    in each lane's registers, so one K/V element read from shared memory
+//  * bf16 pools with head_dim 64 or 128 and 8 KV heads (one warp each) run
+//    both products on the tensor cores with mma.sync m16n8k16 (fp32
+//    accumulate): the group's query heads are the rows of a 16-row tile, a
+//    block's 16 tokens its columns (Q K^T) and its reduction dimension (P V),
+//    the softmax runs on the accumulator fragments and P is re-packed from
+//    them as the A operand. A block's token rows are copied in groups of 4
+//    with 16 bytes of padding after each group so that the ldmatrix reads
+//    of one KV head's tokens spread over the banks.
+//  * Otherwise (fp32, head_dim 256, fewer KV heads) the products run on the
+//    CUDA cores. Warp w serves KV head w % Hkv (and 1/WH of each block's
+//    tokens when a KV head has WH > 1 warps). Up to four query heads of the
+//    GQA group live in each lane's registers, so one K/V element read from shared memory
 //    feeds four FMAs; larger groups split their heads over lane groups.
 //    Lanes split a token's head_dim in 16-byte chunks; packed fp32x2 FMAs
 //    (FFMA2) do the dot products and the P.V update.
-//  * Online softmax in the log2 domain (q pre-scaled by scale*log2 e) with a
+//  * Online softmax in the log2 domain (scores scaled by scale*log2 e) with a
 //    lazy running max: the accumulator is rescaled only when a new score
 //    exceeds the running max by more than 8 (weights stay <= 256), decided
 //    per warp so the rescale is a uniform branch. The partial dot products of
 //    a batch are reduce-scattered over the lanes of a token group, so each
 //    score's max, weight and sum are computed by one lane only, and the
 //    weights are gathered back for P.V.
-//  * Tokens past the context (the tail of a last block) are never loaded and
-//    never touched, so stale or NaN slots cannot leak into the result.
+//  * Tokens past the context (the tail of a last block) are never loaded;
+//    their scores are masked and (tensor-core path) their value rows in
+//    shared memory zeroed, so stale or NaN slots cannot leak into the result.
 #pragma once
 #include <algorithm>
 
@@ -133,21 +144,21 @@ struct SmemLayout {
   int stages;
   int tokens_per_unit;  // tokens of one block moved per pipeline stage (16, 8 or 4)
   int parts;            // 16 / tokens_per_unit
-  int pair_pitch;       // bytes from one pair of token rows (all KV heads) to the next
-  int part_bytes;       // one K (or V) part: tokens_per_unit / 2 * pair_pitch
+  int quad_pitch;       // bytes from one group of 4 token rows (all KV heads) to the next
+  int part_bytes;       // one K (or V) part: tokens_per_unit / 4 * quad_pitch
   int off_bars, off_done, off_flags, off_mbars, off_table, off_ntok, off_merge, off_prefix, total;
 };
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline SmemLayout make_layout(int stages, int tokens_per_unit, int hkv, int d,
-                                                  int elt, int wh, int group, int num_seqs, int pair_pad) {
+                                                  int elt, int wh, int group, int num_seqs, int quad_pad) {
   SmemLayout L;
   L.stages = stages;
   L.tokens_per_unit = tokens_per_unit;
   L.parts = kBlockSize / tokens_per_unit;
-  L.pair_pitch = 2 * hkv * d * elt + pair_pad;
-  L.part_bytes = tokens_per_unit / 2 * L.pair_pitch;
+  L.quad_pitch = 4 * hkv * d * elt + quad_pad;
+  L.part_bytes = tokens_per_unit / 4 * L.quad_pitch;
   const int off = stages * 2 * L.part_bytes;
   L.off_bars = align_up(off, 16);
   L.off_done = L.off_bars + stages * 8;
@@ -358,10 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       char* kdst = smem + st * 2 * L.part_bytes;
       mbar_arrive_expect_tx(&bars[st], 2 * bytes);
       if constexpr (C::kMma) {
-        for (int t = 0; t < ntok; t += 2) {
-          const uint32_t b2 = static_cast<uint32_t>(min(2, ntok - t) * kTokenBytes);
-          bulk_g2s(kdst + (t / 2) * L.pair_pitch, p.k_pool + src + t * kTokenBytes, b2, &bars[st]);
-          bulk_g2s(kdst + L.part_bytes + (t / 2) * L.pair_pitch, p.v_pool + src + t * kTokenBytes, b2,
+        for (int t = 0; t < ntok; t += 4) {
+          const uint32_t b2 = static_cast<uint32_t>(min(4, ntok - t) * kTokenBytes);
+          bulk_g2s(kdst + (t / 4) * L.quad_pitch, p.k_pool + src + t * kTokenBytes, b2, &bars[st]);
+          bulk_g2s(kdst + L.part_bytes + (t / 4) * L.quad_pitch, p.v_pool + src + t * kTokenBytes, b2,
                    &bars[st]);
         }
       } else {
@@ -399,20 +410,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     // S fragments in fp32; O (16 rows x D) += P V with P re-packed from the S
     // fragments as the A operand. Rows are the group's query heads (G of 16
     // are real), so lane t owns rows t/4 and t/4 + 8, columns 2(t%4), +1.
-    // Column n of S n-tile j is token 2n + j (the even tokens, then the odd
-    // ones), which keeps every ldmatrix conflict-free on the padded layout;
-    // P V takes its k index in the same order.
+    // Token rows arrive in groups of 4 (one bulk copy each, 16 padding bytes
+    // after each group), so the rows of one group share banks and different
+    // groups do not. Column n of S n-tile j is token 4(n/2) + 2j + n%2: each
+    // ldmatrix matrix takes 2 tokens from each of the 4 groups (2-way bank
+    // conflicts at most); P V takes its k index in the same order.
     const int g = warp;
     const int gi = lane >> 2, qi = lane & 3;
     constexpr int KS = D / 16;
     // ldmatrix row addresses of this lane inside a K / V part (token t sits
-    // at (t / 2) pairs + (t % 2) rows): K matrices are (even | odd tokens) x
-    // (d lo | hi) of a k-step, V (.trans) matrices are (even | odd tokens) x
-    // (d of n-tile 2n | 2n+1)
+    // at t / 4 groups + t % 4 rows): K matrices are (n-tile 0 | 1 tokens) x
+    // (d lo | hi) of a k-step, V (.trans) matrices are (n-tile 0 | 1 tokens)
+    // x (d of n-tile 2n | 2n+1)
     const int lm = lane >> 3, lr = lane & 7;
-    const uint32_t k_lane = static_cast<uint32_t>(lr * L.pair_pitch + (lm >> 1) * kTokenBytes +
+    const uint32_t k_lane = static_cast<uint32_t>((lr / 2) * L.quad_pitch +
+                                                  (2 * (lm >> 1) + lr % 2) * kTokenBytes +
                                                   (g * D + (lm & 1) * 8) * 2);
-    const uint32_t v_lane = static_cast<uint32_t>(lr * L.pair_pitch + (lm & 1) * kTokenBytes +
+    const uint32_t v_lane = static_cast<uint32_t>((lr / 2) * L.quad_pitch +
+                                                  (2 * (lm & 1) + lr % 2) * kTokenBytes +
                                                   (g * D + (lm >> 1) * 8) * 2);
     const uint32_t sbase = smem_addr(smem);
     uint32_t qa[KS][4];
@@ -466,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
             constexpr int kChunkRow = D * 2 / 16;
             for (int i = lane; i < (kBlockSize - ntok) * kChunkRow; i += 32) {
               const int t = ntok + i / kChunkRow;
-              *reinterpret_cast<uint4*>(vrow + (t / 2) * L.pair_pitch + (t % 2) * kTokenBytes +
+              *reinterpret_cast<uint4*>(vrow + (t / 4) * L.quad_pitch + (t % 4) * kTokenBytes +
                                         (i % kChunkRow) * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();  // ordered before the stage's next bulk copy
@@ -488,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const bool valid = 2 * (2 * qi + e) + n < ntok;  // token of column 2qi+e of n-tile n
+              const bool valid = 4 * qi + 2 * n + e < ntok;  // token of column 2qi+e of n-tile n
               sc[n][e] = valid ? sc[n][e] * p.scale_log2 : -INFINITY;
               sc[n][2 + e] = valid ? sc[n][2 + e] * p.scale_log2 : -INFINITY;
               mt0 = fmaxf(mt0, sc[n][e]);
@@ -589,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           uint32_t* orow = reinterpret_cast<uint32_t*>(static_cast<T*>(p.out) +
                                                        (static_cast<int64_t>(row) * p.hq + head) * D);
 #pragma unroll
-          for (int n = 0; n < D / 8; ++n) orow[4 * n + qi] = pack_bf16x2(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
+          for (int n = 0; n < D / 8; ++n)
+            orow[4 * n + qi] = pack_bf16x2(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
         } else {
           const int64_t slot = static_cast<int64_t>(blockIdx.x) + s;
           if (qi == 0) p.ws_ml[slot * p.hq + head] = make_float2(mr, poisoned ? -1.f : lr_);
@@ -1147,8 +1163,8 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   int tpu = kBlockSize;
   while (tpu > 4 && 2 * tpu * token_bytes > 64 * 1024) tpu /= 2;
   const int smem_limit = 227 * 1024 - 1024;  // leave room for static shared memory
-  // the tensor-core path pads every pair of token rows by 16 bytes, so the
-  // even (or the odd) tokens of one KV head fall in different banks
+  // the tensor-core path pads every group of 4 token rows by 16 bytes, so
+  // the 8 tokens of one ldmatrix matrix meet at most 2 to a bank
   const int pad = Cfg<T, D, G, WH>::kMma ? 16 : 0;
   SmemLayout L = make_layout(4, tpu, hkv, D, elt, WH, G, a.num_seqs, pad);
   if (L.total > smem_limit) L = make_layout(3, tpu, hkv, D, elt, WH, G, a.num_seqs, pad);
