@@ -58,7 +58,7 @@ PAGES_CONTEXT = {
 SPEC_HBM_GBS = 7900.0        # HBM3e
 SPEC_BF16_TFLOPS = 2250.0    # dense bf16 tensor
 
-NCU_DECODE_TRAFFIC = {"bytes": 641539840, "src_sha": "d103752b550b9544"}
+NCU_DECODE_TRAFFIC = {"bytes": 641513472, "src_sha": "373cf9e227e18236"}
 
 
 def _src_sha(path: str) -> str:
