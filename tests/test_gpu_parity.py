@@ -87,12 +87,14 @@ def test_decode_tiny_f32():
     assert int(db.status.item()) == 0, info
 
 
+@pytest.mark.parametrize("hkv", [4, 8])
 @pytest.mark.parametrize("ctas", [1, 3, 64, 1024])
-def test_decode_split_counts(ctas):
+def test_decode_split_counts(ctas, hkv):
     """Every CTA count gives the same result within tolerance, including a
-    count far above the number of blocks (empty CTAs, many partials)."""
-    w = W.paged_workload("split", 5, [1, 15, 16, 17, 33, 100, 257, 600], [1] * 8, 16, 4, 128, 200,
-                         torch.bfloat16, write_new=True)
+    count far above the number of blocks (empty CTAs, many partials); 8 KV
+    heads take the tensor-core products, 4 the CUDA-core ones."""
+    w = W.paged_workload("split", 5, [1, 15, 16, 17, 33, 100, 257, 600], [1] * 8, 4 * hkv, hkv, 128,
+                         200, torch.bfloat16, write_new=True)
     pa.pa_set_decode_ctas(ctas)
     out, db = run_decode(w)
     compare(out, oracle_out(w), torch.bfloat16)
@@ -119,6 +121,8 @@ def test_decode_cta_range_beyond_table_cache(dtype):
     (64, 8, 8, torch.bfloat16), (64, 16, 2, torch.float32), (128, 8, 1, torch.bfloat16),
     (128, 16, 4, torch.float32), (256, 16, 8, torch.bfloat16), (256, 8, 1, torch.float32),
     (128, 64, 8, torch.bfloat16), (256, 32, 4, torch.bfloat16),
+    # tensor-core products (bf16, head_dim 64 / 128, 8 KV heads): every group size
+    (128, 16, 8, torch.bfloat16), (64, 32, 8, torch.bfloat16), (64, 64, 8, torch.bfloat16),
 ])
 def test_decode_shapes(d, hq, hkv, dtype):
     w = W.paged_workload("shape", 11, [3, 16, 31, 200, 513], [1] * 5, hq, hkv, d, 128, dtype,
@@ -159,8 +163,9 @@ def test_decode_permutation_bit_identical():
     assert torch.equal(out_a, out_b)
 
 
-def test_decode_bad_block_and_length_zeroed():
-    w = W.paged_workload("bad", 2, [40, 40, 40], [1, 1, 1], 8, 2, 64, 32, torch.float32,
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(8, 2, 64, torch.float32), (32, 8, 128, torch.bfloat16)])
+def test_decode_bad_block_and_length_zeroed(hq, hkv, d, dtype):
+    w = W.paged_workload("bad", 2, [40, 40, 40], [1, 1, 1], hq, hkv, d, 32, dtype,
                          write_new=False)
     bt = w.block_tables.clone()
     bt[1, 1] = w.num_blocks + 5
@@ -174,7 +179,7 @@ def test_decode_bad_block_and_length_zeroed():
     assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[2]) == 0
     good = oracle.paged_attention(w.q[:1], w.k_pool, w.v_pool, torch.tensor([0, 1], dtype=torch.int32),
                                   w.context_lens[:1], w.block_tables[:1], w.scale)
-    compare(out[:1], good, torch.float32)
+    compare(out[:1], good, dtype)
 
 
 def test_decode_empty_batch():
