@@ -20,8 +20,8 @@
 //    any relabelling of physical blocks or sharing of blocks.
 //  * A pool block stores its 16 tokens x all KV heads contiguously, so one
 //    1-D bulk copy (cp.async.bulk) moves a whole block of K (and one of V)
-//    into shared memory: 16-byte aligned, fully coalesced (four copies of 4
-//    token rows each on the tensor-core path below). A 3-4 stage
+//    into shared memory: 16-byte aligned, fully coalesced (TMA boxes on the
+//    tensor-core path below). A 3-4 stage
 //    mbarrier pipeline keeps >= 2 blocks (up to 128 KB) in flight per SM. The
 //    CTA's slice of the block tables is staged in shared memory up front.
 //  * Warps are decoupled: each waits only on the stage it reads, and the last
@@ -32,9 +32,9 @@
 //    accumulate): the group's query heads are the rows of a 16-row tile, a
 //    block's 16 tokens its columns (Q K^T) and its reduction dimension (P V),
 //    the softmax runs on the accumulator fragments and P is re-packed from
-//    them as the A operand. A block's token rows are copied in groups of 4
-//    with 16 bytes of padding after each group so that the ldmatrix reads
-//    of one KV head's tokens spread over the banks.
+//    them as the A operand. A block moves as one 4-D TMA box per 64 columns
+//    of head_dim that lands as [head][token][64 elements] with 128-byte
+//    swizzle, so the ldmatrix reads of one KV head's tokens hit every bank.
 //  * Otherwise (fp32, head_dim 256, fewer KV heads) the products run on the
 //    CUDA cores. Warp w serves KV head w % Hkv (and 1/WH of each block's
 //    tokens when a KV head has WH > 1 warps). Up to four query heads of the
@@ -49,14 +49,16 @@
 //    a batch are reduce-scattered over the lanes of a token group, so each
 //    score's max, weight and sum are computed by one lane only, and the
 //    weights are gathered back for P.V.
-//  * Tokens past the context (the tail of a last block) are never loaded;
-//    their scores are masked and (tensor-core path) their value rows in
-//    shared memory zeroed, so stale or NaN slots cannot leak into the result.
+//  * Tokens past the context (the tail of a last block) are never loaded by
+//    the CUDA-core path; the tensor-core path loads the whole block, masks
+//    their scores and zeroes their value rows in shared memory. Either way
+//    stale or NaN slots cannot leak into the result.
 #pragma once
 #include <algorithm>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "tmap.h"
 
 namespace pa {
 namespace {
@@ -70,6 +72,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 4-D tiled TMA copy global -> shared, completing its bytes on `bar`.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* tmap, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+      : "memory");
 }
 
 // ldmatrix: four 8 x 8 bf16 matrices; lanes 8i .. 8i+7 give the row
@@ -144,21 +156,19 @@ struct SmemLayout {
   int stages;
   int tokens_per_unit;  // tokens of one block moved per pipeline stage (16, 8 or 4)
   int parts;            // 16 / tokens_per_unit
-  int quad_pitch;       // bytes from one group of 4 token rows (all KV heads) to the next
-  int part_bytes;       // one K (or V) part: tokens_per_unit / 4 * quad_pitch
+  int part_bytes;       // one K (or V) part: tokens_per_unit * Hkv * D * elt
   int off_bars, off_done, off_flags, off_mbars, off_table, off_ntok, off_merge, off_prefix, total;
 };
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline SmemLayout make_layout(int stages, int tokens_per_unit, int hkv, int d,
-                                                  int elt, int wh, int group, int num_seqs, int quad_pad) {
+                                                  int elt, int wh, int group, int num_seqs) {
   SmemLayout L;
   L.stages = stages;
   L.tokens_per_unit = tokens_per_unit;
   L.parts = kBlockSize / tokens_per_unit;
-  L.quad_pitch = 4 * hkv * d * elt + quad_pad;
-  L.part_bytes = tokens_per_unit / 4 * L.quad_pitch;
+  L.part_bytes = tokens_per_unit * hkv * d * elt;
   const int off = stages * 2 * L.part_bytes;
   L.off_bars = align_up(off, 16);
   L.off_done = L.off_bars + stages * 8;
@@ -169,7 +179,7 @@ __host__ __device__ inline SmemLayout make_layout(int stages, int tokens_per_uni
   L.off_merge = align_up(L.off_ntok + kTableCache, 16);
   const int merge_bytes = (wh - 1) * hkv * group * (d + 2) * 4;
   L.off_prefix = align_up(L.off_merge + merge_bytes, 16);
-  L.total = align_up(L.off_prefix + (num_seqs + 1) * 4, 128);
+  L.total = align_up(L.off_prefix + (num_seqs + 1) * 4, 128) + 1024;  // + base alignment
   return L;
 }
 
@@ -199,6 +209,9 @@ struct DecodeParams {
   int num_groups;
   const float2* pre_ml;  // [num_seqs, hq]
   const float* pre_acc;  // [num_seqs, hq, D]
+  // tensor-core path: the K and V pools as 4-D maps (see make_tmap_pool_heads)
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
 };
 
 // Leading blocks of sequence s whose attention is already in its group's
@@ -273,10 +286,12 @@ __device__ __forceinline__ float merge_factor(float m, float mn) {
 }
 
 template <typename T, int D, int G, int WH>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = Cfg<T, D, G, WH>;
   constexpr int HKV = C::kHkv;
-  extern __shared__ __align__(128) char smem[];
+  extern __shared__ __align__(128) char smem_raw[];
+  // 1024-byte aligned base (128-byte swizzled TMA boxes need it)
+  char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const SmemLayout& L = p.L;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
   int* done = reinterpret_cast<int*>(smem + L.off_done);
@@ -367,15 +382,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       const uint32_t bytes = static_cast<uint32_t>(ntok * kTokenBytes);
       const int64_t src = (static_cast<int64_t>(phys) * kBlockSize + part * tpu) * kTokenBytes;
       char* kdst = smem + st * 2 * L.part_bytes;
-      mbar_arrive_expect_tx(&bars[st], 2 * bytes);
       if constexpr (C::kMma) {
-        for (int t = 0; t < ntok; t += 4) {
-          const uint32_t b2 = static_cast<uint32_t>(min(4, ntok - t) * kTokenBytes);
-          bulk_g2s(kdst + (t / 4) * L.quad_pitch, p.k_pool + src + t * kTokenBytes, b2, &bars[st]);
-          bulk_g2s(kdst + L.part_bytes + (t / 4) * L.quad_pitch, p.v_pool + src + t * kTokenBytes, b2,
-                   &bars[st]);
+        // the whole block, one 16 KB box per 64 columns of head_dim: [head][token][64]
+        // with 128-byte swizzle; slots past the context come along and are masked
+        constexpr uint32_t kBox = 64 * kBlockSize * HKV * 2;
+        mbar_arrive_expect_tx(&bars[st], 2 * (D / 64) * kBox);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_4d(kdst + h * kBox, &p.tm_k, 64 * h, 0, 0, phys, &bars[st]);
+          tma_load_4d(kdst + L.part_bytes + h * kBox, &p.tm_v, 64 * h, 0, 0, phys, &bars[st]);
         }
       } else {
+        mbar_arrive_expect_tx(&bars[st], 2 * bytes);
         bulk_g2s(kdst, p.k_pool + src, bytes, &bars[st]);
         bulk_g2s(kdst + L.part_bytes, p.v_pool + src, bytes, &bars[st]);
       }
@@ -410,25 +428,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     // S fragments in fp32; O (16 rows x D) += P V with P re-packed from the S
     // fragments as the A operand. Rows are the group's query heads (G of 16
     // are real), so lane t owns rows t/4 and t/4 + 8, columns 2(t%4), +1.
-    // Token rows arrive in groups of 4 (one bulk copy each, 16 padding bytes
-    // after each group), so the rows of one group share banks and different
-    // groups do not. Column n of S n-tile j is token 4(n/2) + 2j + n%2: each
-    // ldmatrix matrix takes 2 tokens from each of the 4 groups (2-way bank
-    // conflicts at most); P V takes its k index in the same order.
+    // A block arrives as one TMA box per 64 columns of head_dim, laid out
+    // [head][token][64 elements] with 128-byte swizzle (the 16-byte chunk
+    // index XOR the token's row within its 8-row atom), so the 8 tokens of
+    // one ldmatrix matrix hit 8 different bank groups.
     const int g = warp;
     const int gi = lane >> 2, qi = lane & 3;
     constexpr int KS = D / 16;
-    // ldmatrix row addresses of this lane inside a K / V part (token t sits
-    // at t / 4 groups + t % 4 rows): K matrices are (n-tile 0 | 1 tokens) x
-    // (d lo | hi) of a k-step, V (.trans) matrices are (n-tile 0 | 1 tokens)
-    // x (d of n-tile 2n | 2n+1)
+    constexpr uint32_t kBox = 64 * kBlockSize * HKV * 2;
+    // ldmatrix rows of this lane: K matrices are (tokens 0-7 | 8-15) x
+    // (d lo | hi) of a k-step, V (.trans) matrices are (tokens 0-7 | 8-15) x
+    // (d of n-tile 2n | 2n+1); column n of S n-tile j is token 8j + n
     const int lm = lane >> 3, lr = lane & 7;
-    const uint32_t k_lane = static_cast<uint32_t>((lr / 2) * L.quad_pitch +
-                                                  (2 * (lm >> 1) + lr % 2) * kTokenBytes +
-                                                  (g * D + (lm & 1) * 8) * 2);
-    const uint32_t v_lane = static_cast<uint32_t>((lr / 2) * L.quad_pitch +
-                                                  (2 * (lm & 1) + lr % 2) * kTokenBytes +
-                                                  (g * D + (lm >> 1) * 8) * 2);
+    const int tk = (lm >> 1) * 8 + lr, tv = (lm & 1) * 8 + lr;
+    const uint32_t k_row = static_cast<uint32_t>((g * kBlockSize + tk) * 128);
+    const uint32_t v_row = static_cast<uint32_t>((g * kBlockSize + tv) * 128);
     const uint32_t sbase = smem_addr(smem);
     uint32_t qa[KS][4];
     float o[D / 8][4];
@@ -477,12 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           if (ntok < kBlockSize) {
             // rows past the context were not copied and may hold anything:
             // zero this head's slice of the value rows (their weight is 0)
-            char* vrow = smem + st * 2 * L.part_bytes + L.part_bytes + g * D * 2;
-            constexpr int kChunkRow = D * 2 / 16;
+            char* vpart = smem + st * 2 * L.part_bytes + L.part_bytes;
+            constexpr int kChunkRow = D * 2 / 16;  // 16-byte chunks of one row over all boxes
             for (int i = lane; i < (kBlockSize - ntok) * kChunkRow; i += 32) {
-              const int t = ntok + i / kChunkRow;
-              *reinterpret_cast<uint4*>(vrow + (t / 4) * L.quad_pitch + (t % 4) * kTokenBytes +
-                                        (i % kChunkRow) * 16) = make_uint4(0u, 0u, 0u, 0u);
+              const int t = ntok + i / kChunkRow, c = i % kChunkRow;
+              *reinterpret_cast<uint4*>(vpart + (c / 8) * kBox + (g * kBlockSize + t) * 128 + (c % 8) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();  // ordered before the stage's next bulk copy
             __syncwarp();
@@ -493,7 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 #pragma unroll
           for (int kk = 0; kk < KS; ++kk) {
             uint32_t kf[4];
-            ldsm_x4(kb + k_lane + kk * 32, kf);
+            const uint32_t c = static_cast<uint32_t>(2 * (kk & 3) + (lm & 1));
+            ldsm_x4(kb + (kk >> 2) * kBox + k_row + ((c ^ (tk & 7)) << 4), kf);
             mma_16816(sc[0], qa[kk], kf[0], kf[1]);
             mma_16816(sc[1], qa[kk], kf[2], kf[3]);
           }
@@ -503,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const bool valid = 4 * qi + 2 * n + e < ntok;  // token of column 2qi+e of n-tile n
+              const bool valid = 8 * n + 2 * qi + e < ntok;  // token of column 2qi+e of n-tile n
               sc[n][e] = valid ? sc[n][e] * p.scale_log2 : -INFINITY;
               sc[n][2 + e] = valid ? sc[n][2 + e] * p.scale_log2 : -INFINITY;
               mt0 = fmaxf(mt0, sc[n][e]);
@@ -547,7 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 #pragma unroll
           for (int np = 0; np < KS; ++np) {
             uint32_t vf[4];
-            ldsm_x4_trans(vb + v_lane + np * 32, vf);
+            const uint32_t c = static_cast<uint32_t>(2 * (np & 3) + (lm >> 1));
+            ldsm_x4_trans(vb + (np >> 2) * kBox + v_row + ((c ^ (tv & 7)) << 4), vf);
             mma_16816(o[2 * np], pa, vf[0], vf[1]);
             mma_16816(o[2 * np + 1], pa, vf[2], vf[3]);
           }
@@ -1163,12 +1179,9 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   int tpu = kBlockSize;
   while (tpu > 4 && 2 * tpu * token_bytes > 64 * 1024) tpu /= 2;
   const int smem_limit = 227 * 1024 - 1024;  // leave room for static shared memory
-  // the tensor-core path pads every group of 4 token rows by 16 bytes, so
-  // the 8 tokens of one ldmatrix matrix meet at most 2 to a bank
-  const int pad = Cfg<T, D, G, WH>::kMma ? 16 : 0;
-  SmemLayout L = make_layout(4, tpu, hkv, D, elt, WH, G, a.num_seqs, pad);
-  if (L.total > smem_limit) L = make_layout(3, tpu, hkv, D, elt, WH, G, a.num_seqs, pad);
-  if (L.total > smem_limit) L = make_layout(2, tpu, hkv, D, elt, WH, G, a.num_seqs, pad);
+  SmemLayout L = make_layout(4, tpu, hkv, D, elt, WH, G, a.num_seqs);
+  if (L.total > smem_limit) L = make_layout(3, tpu, hkv, D, elt, WH, G, a.num_seqs);
+  if (L.total > smem_limit) L = make_layout(2, tpu, hkv, D, elt, WH, G, a.num_seqs);
   if (L.total > smem_limit) return cudaErrorInvalidValue;
 
   int grid = a.grid_override > 0 ? a.grid_override : device_sm_count();
@@ -1202,6 +1215,11 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   p.num_groups = a.num_groups;
   p.pre_ml = static_cast<const float2*>(a.pre_ml);
   p.pre_acc = static_cast<const float*>(a.pre_acc);
+  if constexpr (Cfg<T, D, G, WH>::kMma) {
+    if (!make_tmap_pool_heads(&p.tm_k, a.pool.k, D, hkv, static_cast<uint64_t>(a.pool.num_blocks)) ||
+        !make_tmap_pool_heads(&p.tm_v, a.pool.v, D, hkv, static_cast<uint64_t>(a.pool.num_blocks)))
+      return cudaErrorInvalidValue;
+  }
 
   auto kern = decode_kernel<T, D, G, WH>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);

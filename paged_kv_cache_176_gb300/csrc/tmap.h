@@ -44,4 +44,21 @@ inline bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 paged pool [blocks][16 tokens][heads][d] seen as the 4-D tensor
+// {d, token, head, block}: a box {64, 16, heads, 1} lands in shared memory as
+// [head][token][64 elements], one KV head's 16 token rows contiguous, with
+// 128-byte swizzle.
+inline bool make_tmap_pool_heads(CUtensorMap* map, const void* base, uint64_t d, uint64_t heads,
+                                 uint64_t blocks) {
+  EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {d, 16, heads, blocks};
+  const cuuint64_t strides[3] = {heads * d * 2, d * 2, 16 * heads * d * 2};  // bytes, dims 1..3
+  const cuuint32_t box[4] = {64, 16, static_cast<cuuint32_t>(heads), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace pa
