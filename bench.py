@@ -58,7 +58,7 @@ PAGES_CONTEXT = {
 SPEC_HBM_GBS = 7900.0        # HBM3e
 SPEC_BF16_TFLOPS = 2250.0    # dense bf16 tensor
 
-NCU_DECODE_TRAFFIC = {"bytes": 641513472, "src_sha": "373cf9e227e18236"}
+NCU_DECODE_TRAFFIC = {"bytes": 643954176, "src_sha": "59766216f8efb35b"}
 
 
 def _src_sha(path: str) -> str:
