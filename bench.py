@@ -58,7 +58,7 @@ PAGES_CONTEXT = {
 SPEC_HBM_GBS = 7900.0        # HBM3e
 SPEC_BF16_TFLOPS = 2250.0    # dense bf16 tensor
 
-NCU_DECODE_TRAFFIC = {"bytes": 643954176, "src_sha": "59766216f8efb35b"}
+NCU_DECODE_TRAFFIC = {"bytes": 643954176, "src_sha": "9ae59d780c473911"}
 
 
 def _src_sha(path: str) -> str:

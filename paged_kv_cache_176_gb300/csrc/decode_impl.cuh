@@ -489,8 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           const uint32_t kb = sbase + static_cast<uint32_t>(st * 2 * L.part_bytes);
           const uint32_t vb = kb + static_cast<uint32_t>(L.part_bytes);
           if (ntok < kBlockSize) {
-            // rows past the context were not copied and may hold anything:
-            // zero this head's slice of the value rows (their weight is 0)
+            // slots past the context hold stale or poisoned values: zero this
+            // head's value rows there (their weight is 0, and 0 x NaN is NaN)
             char* vpart = smem + st * 2 * L.part_bytes + L.part_bytes;
             constexpr int kChunkRow = D * 2 / 16;  // 16-byte chunks of one row over all boxes
             for (int i = lane; i < (kBlockSize - ntok) * kChunkRow; i += 32) {
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
               *reinterpret_cast<uint4*>(vpart + (c / 8) * kBox + (g * kBlockSize + t) * 128 + (c % 8) * 16) =
                   make_uint4(0u, 0u, 0u, 0u);
             }
-            fence_proxy_async_smem();  // ordered before the stage's next bulk copy
+            fence_proxy_async_smem();  // ordered before the stage's next TMA copy
             __syncwarp();
           }
           float sc[2][4];
