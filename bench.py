@@ -38,10 +38,6 @@ MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# DRAM bytes (read + write) of one pa_decode call (decode_kernel +
-# decode_reduce_kernel) on the decode batch, from an ncu capture
-# (profiles/decode_b64_bf16.md), valid for the kernel source whose sha256
-# prefix is given; reported as null once the source changes.
 # The source pages' own figures: other hardware, whole-model serving, none a
 # kernel number for this path; quoted beside the measurements as context only.
 PAGES_CONTEXT = {
@@ -58,6 +54,11 @@ PAGES_CONTEXT = {
 SPEC_HBM_GBS = 7900.0        # HBM3e
 SPEC_BF16_TFLOPS = 2250.0    # dense bf16 tensor
 
+# DRAM bytes (read + write) of one pa_decode call (decode_kernel +
+# decode_reduce_kernel) on the decode batch, from an ncu capture of
+# `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`, valid for the
+# kernel source whose sha256 prefix is given; reported as null once the
+# source changes.
 NCU_DECODE_TRAFFIC = {"bytes": 643954176, "src_sha": "9ae59d780c473911"}
 
 
@@ -79,14 +80,15 @@ def peaks() -> dict:
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every ``interval_ms``."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines: list[str] = []
         self._t = None
@@ -95,7 +97,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
@@ -133,7 +135,8 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "interval_ms": self.interval_ms}
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -214,16 +217,22 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    n_ev = min(args.steps, 200)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n_ev)]
-    for a, b in ev:
-        pa.pa_reshape_and_cache(kp, vp, kn, vn, sm, stream=stream)
-        a.record(stream)
-        pa.pa_decode(out, q, kp, vp, bt, cl, w.scale, workspace=ws, stream=stream)
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    decode_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    # events around every pa_decode call, in batches of 200 calls, until at
+    # least 1 s of calls has run (whatever --steps is); clocks sampled meanwhile
+    roof_clocks = ClockSampler(dev.index).start()
+    times, t_start = [], time.perf_counter()
+    while time.perf_counter() - t_start < 1.0 or len(times) < 200:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(200)]
+        for a, b in ev:
+            pa.pa_reshape_and_cache(kp, vp, kn, vn, sm, stream=stream)
+            a.record(stream)
+            pa.pa_decode(out, q, kp, vp, bt, cl, w.scale, workspace=ws, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        times += [a.elapsed_time(b) for a, b in ev]
+    roof_clk = roof_clocks.stop()
+    decode_ms = statistics.median(times)
     gather = gather_ceiling(w, kp, vp, dev, stream)
 
     # timed region: exactly K steps
@@ -383,6 +392,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                      "frac_of_spec": round(decode_gbs / SPEC_HBM_GBS, 4),
                      "spec_peak": SPEC_HBM_GBS,
                      "peak_source": pk["source"], "ms_per_launch": round(decode_ms, 5),
+                     "launches_timed": len(times), "clocks": roof_clk,
                      "gather_ceiling": dict(gather, decode_frac_of_ceiling=round(
                          decode_gbs / gather["gbs"], 4)),
                      "algorithmic_bytes_per_launch": nb["decode"]},

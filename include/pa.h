@@ -11,7 +11,9 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Pointers marked "device" are CUDA device pointers owned by the caller; the
- *    library allocates no memory and keeps no state between calls.
+ *    library allocates no memory and keeps no state between calls that could
+ *    change a result (it caches only per-device facts: the SM count, and the
+ *    address of pa_decode_static_ws's array).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream). PA_OK means "validated and enqueued".
  *  - Host-side validation looks only at scalars and pointer values; on any
@@ -21,6 +23,9 @@
  *    the device: the kernel ORs a PA_STATUS_* bit into *d_status (when
  *    d_status is not NULL), skips the bad access and writes zeros for the
  *    affected output rows. Nothing traps.
+ *  - Every wait of a kernel on an asynchronous copy is bounded (2 s); if one
+ *    gives up, the kernel ORs PA_STATUS_TIMEOUT into *d_status, stops, and
+ *    the call's outputs are undefined.
  *  - Layouts are row-major and contiguous:
  *      K/V pool     [num_blocks, block_size, num_kv_heads, head_dim]
  *      q, out       [num_tokens, num_q_heads, head_dim]
@@ -149,8 +154,15 @@ PA_API int pa_decode(const pa_kv_pool* pool, void* out, const void* q, int num_s
  *    (cudaGetSymbolAddress, with that device current) and caches it; make the
  *    first call on a device before any stream capture.
  *  - Every call uses the same array, which keeps the previous call's
- *    contents; nothing in it needs to start at zero. Calls that overlap on the
- *    GPU (other streams, other host threads) race on it: serialize them.
+ *    contents; nothing in it needs to start at zero (a call whose status gets
+ *    PA_STATUS_TIMEOUT has undefined outputs, as for every entry point).
+ *    Calls that overlap on the GPU (other streams, other host threads) race
+ *    on it: serialize them.
+ *  - The cached address is that of the device's context at the first call;
+ *    after cudaDeviceReset on a device, do not call this entry point on it
+ *    again in the same process.
+ *  - Argument errors return what pa_decode would return; the size limit is
+ *    checked after them.
  */
 #define PA_DECODE_STATIC_WS_BYTES (((size_t)32) << 20)
 PA_API int pa_decode_static_ws(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
@@ -203,13 +215,25 @@ PA_API int pa_decode_cascade(const pa_kv_pool* pool, void* out, const void* q, i
                              void* workspace, size_t workspace_bytes, int* d_status, void* stream);
 
 /*
- * Tuning knob: the number of persistent CTAs the decode kernel runs (0, the
- * default, means one per SM of the current device; values above 1024 are
- * clamped). It applies to later pa_decode / pa_mixed_step calls from any
- * thread. Returns the previous value. Results do not depend on it beyond
- * floating-point summation order.
+ * pa_decode and pa_decode_cascade with an explicit number of persistent
+ * decode CTAs instead of the default of one per SM of the current device
+ * (num_ctas == 0 keeps the default; values above 1024 are clamped; negative
+ * values return PA_EINVAL). The CTA count sets where the balanced split-K
+ * cuts the batch's blocks, so it changes the floating-point summation order
+ * and nothing else. For tuning and for tests that make sequences straddle
+ * many CTAs; the count is an argument, never library state.
  */
-PA_API int pa_set_decode_ctas(int num_ctas);
+PA_API int pa_decode_with_ctas(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+                               int num_q_heads, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* context_lens, float scale,
+                               int num_ctas, void* workspace, size_t workspace_bytes,
+                               int* d_status, void* stream);
+PA_API int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q,
+                                       int num_seqs, int num_q_heads, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       const int32_t* cu_groups, const int32_t* prefix_lens,
+                                       int num_groups, float scale, int num_ctas, void* workspace,
+                                       size_t workspace_bytes, int* d_status, void* stream);
 
 /* Bytes of workspace pa_mixed_step needs for these sizes (0 on invalid sizes). */
 PA_API size_t pa_mixed_workspace_size(int num_seqs, int num_tokens, int num_q_heads, int head_dim,

@@ -1,6 +1,7 @@
 /*
- * pa_probe.h -- a measurement aid, not part of the attention path; the pages
- * have no counterpart for it.
+ * pa_probe.h -- measurement and test aids, not part of the attention path;
+ * the pages have no counterpart for them. They live in their own library,
+ * libpa_probe.so, next to libpa.so.
  *
  * pa_gather_probe streams whole K and V blocks of a paged pool into shared
  * memory with the same machinery the decode kernel uses (persistent CTAs, a
@@ -33,6 +34,27 @@ extern "C" {
 
 PA_API int pa_gather_probe(const pa_kv_pool* pool, const int32_t* blocks, int n, int stages,
                            int ctas, int* d_status, void* stream);
+
+/*
+ * pa_wait_probe runs, in one CTA, the bounded wait and give-up path that every
+ * libpa kernel takes when an asynchronous copy does not complete, without
+ * leaving anything in flight: a warp holds 32 TMEM columns, thread 0 arms an
+ * mbarrier for a 1,024-byte bulk copy, and every thread waits on it for at
+ * most limit_ns of global time.
+ *
+ *  src       device, 16-byte aligned, >= 1,024 bytes: the copy's source
+ *  starve    0: the copy is issued, the wait completes, the copied bytes are
+ *            checked (PA_STATUS_BAD_BLOCK on a mismatch);
+ *            1: the barrier is armed but the copy never started, so the wait
+ *            runs out: the kernel ORs PA_STATUS_TIMEOUT into *d_status,
+ *            releases its TMEM and returns
+ *  limit_ns  1 .. 2e9 (the kernels' own limit); PA_EINVAL otherwise
+ *  d_status  device int, nullable
+ *
+ * Asynchronous on `stream`; returns a pa_status.
+ */
+PA_API int pa_wait_probe(const void* src, int starve, unsigned long long limit_ns, int* d_status,
+                         void* stream);
 
 #ifdef __cplusplus
 }

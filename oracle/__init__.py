@@ -46,6 +46,9 @@ def _setup(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_reshape_and_cache.restype = ctypes.c_int
     lib.oracle_reshape_and_cache.argtypes = [P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                                              P, P, P, ctypes.c_int]
+    lib.oracle_copy_blocks.restype = ctypes.c_int
+    lib.oracle_copy_blocks.argtypes = [P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int64, P, P, P,
+                                       ctypes.c_int]
     lib.oracle_paged_attention.restype = ctypes.c_int
     lib.oracle_paged_attention.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -129,6 +132,37 @@ def _writeback(dst, src: np.ndarray) -> None:
                 view[...] = src
     except ImportError:  # pragma: no cover
         pass
+
+
+def copy_blocks(k_pool, v_pool, src, dst, ntok=None, lib=None) -> int:
+    """In-place copy-on-write copy on host pools ``[N_blk, b, Hkv, d]``: pair i
+    copies the first ``ntok[i]`` slots (whole blocks when ``ntok`` is None) of
+    block ``src[i]`` onto block ``dst[i]``. Returns 0, or ORACLE_ERANGE (2)
+    when a bad pair was skipped."""
+    lib = lib or load()
+    kp, vp = _raw(k_pool), _raw(v_pool)
+    s = np.ascontiguousarray(_raw(src), dtype=np.int32)
+    d = np.ascontiguousarray(_raw(dst), dtype=np.int32)
+    n = None if ntok is None else np.ascontiguousarray(_raw(ntok), dtype=np.int32)
+    nb, b = kp.shape[0], kp.shape[1]
+    token_bytes = int(np.prod(kp.shape[2:])) * kp.itemsize
+    rc = lib.oracle_copy_blocks(_ptr(kp), _ptr(vp), nb, b, token_bytes, _ptr(s), _ptr(d), _ptr(n),
+                                int(s.shape[0]))
+    if rc not in (0, 2):
+        raise ValueError(f"oracle_copy_blocks failed with code {rc}")
+    for dst_t, src_a in ((k_pool, kp), (v_pool, vp)):
+        _writeback(dst_t, src_a)
+    return int(rc)
+
+
+def cow_write(k_pool, v_pool, k_new, v_new, slot_mapping, src, dst, ntok, lib=None) -> int:
+    """The fused copy-on-write KV write on host pools: the copies first (the
+    filled slots of each shared block onto its fresh copy), then the step's
+    KV write into the copies and other blocks. Returns copy_blocks' code."""
+    rc = copy_blocks(k_pool, v_pool, src, dst, ntok, lib=lib)
+    if slot_mapping is not None and len(slot_mapping):
+        reshape_and_cache(k_pool, v_pool, k_new, v_new, slot_mapping, lib=lib)
+    return rc
 
 
 def paged_attention(q, k_pool, v_pool, cu_q_lens, context_lens, block_tables, scale: float,

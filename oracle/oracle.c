@@ -46,6 +46,30 @@ int oracle_reshape_and_cache(void* k_pool, void* v_pool, int64_t num_blocks,
   return ORACLE_OK;
 }
 
+int oracle_copy_blocks(void* k_pool, void* v_pool, int64_t num_blocks,
+                       int block_size, int64_t token_bytes,
+                       const int32_t* src, const int32_t* dst,
+                       const int32_t* ntok, int n) {
+  if (!k_pool || !v_pool || block_size <= 0 || token_bytes <= 0 || n < 0 ||
+      (n > 0 && (!src || !dst)))
+    return ORACLE_EARG;
+  int status = ORACLE_OK;
+  const int64_t block_bytes = (int64_t)block_size * token_bytes;
+  for (int i = 0; i < n; ++i) {
+    int64_t from = src[i], to = dst[i];
+    int slots = ntok ? ntok[i] : block_size; /* the filled part of the block */
+    if (from < 0 || from >= num_blocks || to < 0 || to >= num_blocks ||
+        slots < 0 || slots > block_size) {
+      status = ORACLE_ERANGE; /* skipped */
+      continue;
+    }
+    size_t bytes = (size_t)(slots * token_bytes);
+    memcpy((char*)k_pool + to * block_bytes, (const char*)k_pool + from * block_bytes, bytes);
+    memcpy((char*)v_pool + to * block_bytes, (const char*)v_pool + from * block_bytes, bytes);
+  }
+  return status;
+}
+
 typedef struct {
   double* out;
   const void* q;

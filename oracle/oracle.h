@@ -15,6 +15,15 @@
  *    example of "Inference engine core techniques", section 1.2). Slot -1 is
  *    skipped. The copy is byte-exact.
  *
+ *  - oracle_copy_blocks: the copy-on-write copy. Several sequences may point
+ *    their tables at one physical block (the replies of one request share the
+ *    prompt's blocks; beams share their prefix pages); before a sequence
+ *    writes into a shared block, that block is copied and the sequence's
+ *    table points at the copy ("C13 L2 serving", parallel-sampling paragraph;
+ *    "Inference engine core techniques", section 1.5). Pair i copies the
+ *    first ntok[i] token slots (all slots when ntok is NULL) of block src[i]
+ *    onto block dst[i] of both pools, byte for byte, pairs in order.
+ *
  *  - oracle_paged_attention: for every query row, gather the sequence's K/V
  *    through its block table (K_r = gather(K_pool, table_r), the gather figure
  *    of "C13 L2 serving: continuous batching and PagedAttention"), then plain
@@ -55,6 +64,20 @@ int oracle_reshape_and_cache(void* k_pool, void* v_pool, int64_t num_blocks,
                              int block_size, int64_t token_bytes,
                              const void* k_new, const void* v_new,
                              const int64_t* slot_mapping, int num_tokens);
+
+/*
+ * k_pool, v_pool: [num_blocks, block_size, token_bytes] raw bytes.
+ * src, dst:       [n] physical block ids.
+ * ntok:           [n] slots to copy per pair (0..block_size), or NULL for
+ *                 whole blocks.
+ * A pair with an id outside [0, num_blocks) or ntok outside [0, block_size]
+ * is skipped; the others are still applied, and the call then returns
+ * ORACLE_ERANGE.
+ */
+int oracle_copy_blocks(void* k_pool, void* v_pool, int64_t num_blocks,
+                       int block_size, int64_t token_bytes,
+                       const int32_t* src, const int32_t* dst,
+                       const int32_t* ntok, int n);
 
 /*
  * out:          [num_tokens, num_q_heads, head_dim] fp64.

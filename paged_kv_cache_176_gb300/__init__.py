@@ -12,7 +12,8 @@ from .abi import (  # noqa: F401
     pa_mixed_step,
     pa_mixed_workspace_size,
     pa_reshape_and_cache,
-    pa_set_decode_ctas,
+    pa_decode_with_ctas,
+    pa_decode_cascade_with_ctas,
     pa_strerror,
     pa_version,
 )
@@ -25,7 +26,8 @@ __all__ = [
     "pa_decode_workspace_size",
     "pa_mixed_step",
     "pa_mixed_workspace_size",
-    "pa_set_decode_ctas",
+    "pa_decode_with_ctas",
+    "pa_decode_cascade_with_ctas",
     "pa_strerror",
     "pa_version",
     "PagedAttentionError",

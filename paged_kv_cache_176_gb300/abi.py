@@ -16,6 +16,7 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpa.so")
+PROBE_LIB_PATH = os.path.join(_HERE, "libpa_probe.so")
 
 PA_OK = 0
 PA_EINVAL = -1
@@ -80,17 +81,41 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_mixed_workspace_size.argtypes = [I, I, I, I, I]
         lib.pa_mixed_step.restype = I
         lib.pa_mixed_step.argtypes = [PP, P, P, P, I, I, I, P, P, I, F, I, P, P, P, P, SZ, P, P]
-        lib.pa_set_decode_ctas.restype = I
-        lib.pa_set_decode_ctas.argtypes = [I]
+        lib.pa_decode_with_ctas.restype = I
+        lib.pa_decode_with_ctas.argtypes = [PP, P, P, I, I, P, I, P, F, I, P, SZ, P, P]
         lib.pa_decode_static_ws.restype = I
         lib.pa_decode_static_ws.argtypes = [PP, P, P, I, I, P, I, P, F, P, P]
-        lib.pa_gather_probe.restype = I
-        lib.pa_gather_probe.argtypes = [PP, P, I, I, I, P, P]
         lib.pa_decode_cascade_workspace_size.restype = SZ
         lib.pa_decode_cascade_workspace_size.argtypes = [I, I, I, I]
         lib.pa_decode_cascade.restype = I
         lib.pa_decode_cascade.argtypes = [PP, P, P, I, I, P, I, P, P, P, I, F, P, SZ, P, P]
+        lib.pa_decode_cascade_with_ctas.restype = I
+        lib.pa_decode_cascade_with_ctas.argtypes = [PP, P, P, I, I, P, I, P, P, P, I, F, I, P, SZ, P,
+                                                    P]
         _lib = lib
+        return lib
+
+
+_probe_lib: Optional[ctypes.CDLL] = None
+
+
+def load_probe(path: str = PROBE_LIB_PATH) -> ctypes.CDLL:
+    """Load libpa_probe.so, the measurement and test aids of include/pa_probe.h
+    (built beside libpa.so; not part of the attention path)."""
+    global _probe_lib
+    with _lock:
+        if _probe_lib is not None:
+            return _probe_lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m paged_kv_cache_176_gb300.build`")
+        lib = ctypes.CDLL(path)
+        P, I, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong
+        lib.pa_gather_probe.restype = I
+        lib.pa_gather_probe.argtypes = [ctypes.POINTER(pa_kv_pool), P, I, I, I, P, P]
+        lib.pa_wait_probe.restype = I
+        lib.pa_wait_probe.argtypes = [P, I, U64, P, P]
+        _probe_lib = lib
         return lib
 
 
@@ -100,11 +125,6 @@ def pa_strerror(status: int) -> str:
 
 def pa_version() -> int:
     return int(load().pa_version())
-
-
-def pa_set_decode_ctas(n: int) -> int:
-    """Number of persistent decode CTAs (0: one per SM). Returns the old value."""
-    return int(load().pa_set_decode_ctas(int(n)))
 
 
 # ----------------------------------------------------------------- helpers
@@ -200,6 +220,23 @@ def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale: float, 
     return out
 
 
+def pa_decode_with_ctas(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,
+                        num_ctas: int, workspace=None, d_status=None, stream=None):
+    """pa_decode on ``num_ctas`` persistent CTAs (0: one per SM). Returns out."""
+    lib = load()
+    pool = make_pool(k_pool, v_pool)
+    S, hq, d = q.shape
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    mb = int(block_tables.shape[1])
+    ws = _workspace(pa_decode_workspace_size(S, hq, d, mb), q.device, workspace)
+    _check("pa_decode_with_ctas",
+           lib.pa_decode_with_ctas(ctypes.byref(pool), _ptr(out), _ptr(q), S, hq, _ptr(block_tables),
+                                   mb, _ptr(context_lens), float(scale), int(num_ctas), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream)))
+    return out
+
+
 def pa_decode_cascade_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int,
                                     max_blocks_per_seq: int) -> int:
     return int(load().pa_decode_cascade_workspace_size(num_seqs, num_q_heads, head_dim,
@@ -211,6 +248,16 @@ def pa_decode_cascade(out, q, k_pool, v_pool, block_tables, context_lens, cu_gro
     """Decode attention over groups of sequences sharing a prefix of whole
     blocks: sequences cu_groups[g] .. cu_groups[g+1]-1 share their first
     prefix_lens[g] tokens (see include/pa.h). q/out [S, Hq, d]. Returns out."""
+    return pa_decode_cascade_with_ctas(out, q, k_pool, v_pool, block_tables, context_lens,
+                                       cu_groups, prefix_lens, scale, 0, workspace, d_status,
+                                       stream, _name="pa_decode_cascade")
+
+
+def pa_decode_cascade_with_ctas(out, q, k_pool, v_pool, block_tables, context_lens, cu_groups,
+                                prefix_lens, scale: float, num_ctas: int, workspace=None,
+                                d_status=None, stream=None, _name="pa_decode_cascade_with_ctas"):
+    """pa_decode_cascade with ``num_ctas`` persistent decode CTAs (0: one per
+    SM). Returns out."""
     lib = load()
     pool = make_pool(k_pool, v_pool)
     S, hq, d = q.shape
@@ -223,25 +270,40 @@ def pa_decode_cascade(out, q, k_pool, v_pool, block_tables, context_lens, cu_gro
         raise ValueError("cu_groups must hold num_groups + 1 entries")
     mb = int(block_tables.shape[1])
     ws = _workspace(pa_decode_cascade_workspace_size(S, hq, d, mb), q.device, workspace)
-    _check("pa_decode_cascade",
-           lib.pa_decode_cascade(ctypes.byref(pool), _ptr(out), _ptr(q), S, hq, _ptr(block_tables),
-                                 mb, _ptr(context_lens), _ptr(cu_groups), _ptr(prefix_lens), ng,
-                                 float(scale), _ptr(ws), ws.numel() * ws.element_size(),
-                                 _ptr(d_status), _stream(stream)))
+    args = (ctypes.byref(pool), _ptr(out), _ptr(q), S, hq, _ptr(block_tables), mb,
+            _ptr(context_lens), _ptr(cu_groups), _ptr(prefix_lens), ng, float(scale))
+    tail = (_ptr(ws), ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream))
+    if _name == "pa_decode_cascade":
+        rc = lib.pa_decode_cascade(*args, *tail)
+    else:
+        rc = lib.pa_decode_cascade_with_ctas(*args, int(num_ctas), *tail)
+    _check(_name, rc)
     return out
 
 
 def pa_gather_probe(k_pool, v_pool, blocks, stages: int = 3, ctas: int = 0, d_status=None,
                     stream=None) -> None:
-    """Measurement aid (include/pa_probe.h): stream the listed K/V blocks into
-    shared memory with the decode kernel's copies and compute nothing."""
-    lib = load()
+    """Measurement aid (include/pa_probe.h, libpa_probe.so): stream the listed
+    K/V blocks into shared memory with the decode kernel's copies and compute
+    nothing."""
+    lib = load_probe()
     pool = make_pool(k_pool, v_pool)
     if blocks.dtype != torch.int32:
         raise TypeError("blocks must be int32")
     _check("pa_gather_probe", lib.pa_gather_probe(ctypes.byref(pool), _ptr(blocks),
                                                   int(blocks.numel()), stages, ctas,
                                                   _ptr(d_status), _stream(stream)))
+
+
+def pa_wait_probe(src, starve: bool, limit_ns: int, d_status=None, stream=None) -> None:
+    """Test aid (include/pa_probe.h, libpa_probe.so): one CTA through the
+    kernels' bounded wait; with ``starve`` the copy is never started and the
+    wait gives up after ``limit_ns``, setting PA_STATUS_TIMEOUT."""
+    lib = load_probe()
+    if src.numel() * src.element_size() < 1024:
+        raise ValueError("src must hold at least 1,024 bytes")
+    _check("pa_wait_probe", lib.pa_wait_probe(_ptr(src), int(bool(starve)), int(limit_ns),
+                                              _ptr(d_status), _stream(stream)))
 
 
 PA_DECODE_STATIC_WS_BYTES = 32 << 20

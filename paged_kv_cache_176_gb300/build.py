@@ -1,15 +1,22 @@
-"""Build libpa.so (the C-ABI library) from csrc/*.cu with nvcc for sm_103a.
+"""Build libpa.so (the C-ABI library) and libpa_probe.so (its measurement and
+test aids) from csrc/ with nvcc for sm_103a.
 
-Each translation unit compiles in parallel; the objects link into one shared
-library with the CUDA runtime linked statically, so the library loads with
-ctypes and needs nothing but the driver. Outputs stay in-tree:
-``paged_kv_cache_176_gb300/_build/*.o`` and ``paged_kv_cache_176_gb300/libpa.so``.
+Each translation unit compiles in parallel; the objects link into shared
+libraries with the CUDA runtime linked statically, so they load with ctypes
+and need nothing but the driver. Outputs stay in-tree:
+``paged_kv_cache_176_gb300/_build/`` and ``paged_kv_cache_176_gb300/lib*.so``.
+
+A build is reused only when a stamp written beside the objects matches the
+sources, the flags and the host machine's architecture; anything else (a
+changed source, a copy of the tree on another machine) rebuilds.
 """
 from __future__ import annotations
 
 import concurrent.futures as fut
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -18,6 +25,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
+PROBE_LIB = os.path.join(HERE, "libpa_probe.so")
+STAMP = os.path.join(BUILD, "stamp")
 ROOT = os.path.dirname(HERE)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
@@ -31,21 +40,39 @@ def nvcc() -> str:
     return cand
 
 
-def _inputs_mtime() -> float:
-    files = glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
-    files.append(os.path.abspath(__file__))
-    return max(os.path.getmtime(f) for f in files)
+def _sources() -> tuple[list[str], list[str]]:
+    lib = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
+    probe = sorted(glob.glob(os.path.join(CSRC, "probe", "*.cu")))
+    return lib, probe
+
+
+def _stamp(extra_flags) -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(CSRC, "**", "*"), recursive=True)
+                   + glob.glob(os.path.join(ROOT, "include", "*.h")) + [os.path.abspath(__file__)])
+    for f in files:
+        if os.path.isfile(f):
+            h.update(os.path.relpath(f, ROOT).encode())
+            with open(f, "rb") as fh:
+                h.update(fh.read())
+    h.update(" ".join([*ARCH, *NVCC_FLAGS, *extra_flags, platform.machine()]).encode())
+    return h.hexdigest()
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _inputs_mtime():
+    stamp = _stamp(extra_flags)
+    if (not force and os.path.exists(LIB) and os.path.exists(PROBE_LIB) and os.path.exists(STAMP)
+            and open(STAMP).read().strip() == stamp):
+        if verbose:
+            sys.stderr.write("libpa: up to date\n")
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
+    lib_srcs, probe_srcs = _sources()
     exe = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
+        sub = "probe_" if os.path.basename(os.path.dirname(src)) == "probe" else ""
+        obj = os.path.join(BUILD, sub + os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [exe, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -54,14 +81,20 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
+    srcs = lib_srcs + probe_srcs
     with fut.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
-    cmd = [exe, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    for out, o in ((LIB, objs[:len(lib_srcs)]), (PROBE_LIB, objs[len(lib_srcs):])):
+        tmp = out + ".tmp"
+        cmd = [exe, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *o]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, out)
+    with open(STAMP, "w") as f:
+        f.write(stamp + "\n")
+    sys.stderr.write(f"libpa: compiled {len(srcs)} translation units for sm_103a "
+                     f"on {platform.machine()}\n")
     return LIB
 
 

@@ -4,7 +4,6 @@
 // happen in the kernels (see pa.h).
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -32,8 +31,6 @@ int device_sm_count() {
 }
 
 namespace {
-
-std::atomic<int> g_decode_ctas{0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -94,6 +91,25 @@ int validate_kv_write(const pa_kv_pool* pool, const void* k_new, const void* v_n
 }
 
 }  // namespace
+
+int check_decode_args(const pa_kv_pool* pool, const void* out, const void* q, int num_seqs,
+                      int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens) {
+  int rc = check_pool(pool);
+  if (rc != PA_OK) return rc;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0) return PA_EINVAL;
+  rc = check_heads(pool, num_q_heads);
+  if (rc != PA_OK) return rc;
+  if (!decode_supported(pool->dtype, pool->head_dim, num_q_heads / pool->num_kv_heads,
+                        pool->num_kv_heads))
+    return PA_EUNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (out == nullptr || q == nullptr || block_tables == nullptr || context_lens == nullptr)
+    return PA_EINVAL;
+  if (!aligned16(out) || !aligned16(q)) return PA_EINVAL;
+  return PA_OK;
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -113,11 +129,6 @@ const char* pa_strerror(int status) {
 }
 
 int pa_version(void) { return (1 << 16) | 0; }
-
-int pa_set_decode_ctas(int num_ctas) {
-  if (num_ctas < 0) num_ctas = 0;
-  return g_decode_ctas.exchange(num_ctas);
-}
 
 int pa_reshape_and_cache(const pa_kv_pool* pool, const void* k_new, const void* v_new,
                          const int64_t* slot_mapping, int num_tokens, int* d_status,
@@ -141,22 +152,15 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
   return decode_workspace_bytes(num_seqs, num_q_heads, head_dim);
 }
 
-int pa_decode(const pa_kv_pool* pool, void* out, const void* q, int num_seqs, int num_q_heads,
-              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-              float scale, void* workspace, size_t workspace_bytes, int* d_status, void* stream) {
+int pa_decode_with_ctas(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+                        int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* context_lens, float scale, int num_ctas, void* workspace,
+                        size_t workspace_bytes, int* d_status, void* stream) {
   pa::TraceRange trace("pa_decode");
-  int rc = check_pool(pool);
-  if (rc != PA_OK) return rc;
-  if (num_seqs < 0 || max_blocks_per_seq <= 0) return PA_EINVAL;
-  rc = check_heads(pool, num_q_heads);
-  if (rc != PA_OK) return rc;
-  if (!decode_supported(pool->dtype, pool->head_dim, num_q_heads / pool->num_kv_heads,
-                        pool->num_kv_heads))
-    return PA_EUNSUPPORTED;
-  if (num_seqs == 0) return PA_OK;
-  if (out == nullptr || q == nullptr || block_tables == nullptr || context_lens == nullptr)
-    return PA_EINVAL;
-  if (!aligned16(out) || !aligned16(q)) return PA_EINVAL;
+  if (num_ctas < 0) return PA_EINVAL;
+  int rc = check_decode_args(pool, out, q, num_seqs, num_q_heads, block_tables,
+                             max_blocks_per_seq, context_lens);
+  if (rc != PA_OK || num_seqs == 0) return rc;
   const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, pool->head_dim,
                                                max_blocks_per_seq);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PA_EWORKSPACE;
@@ -175,8 +179,15 @@ int pa_decode(const pa_kv_pool* pool, void* out, const void* q, int num_seqs, in
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.d_status = d_status;
-  a.grid_override = g_decode_ctas.load();
+  a.grid_override = num_ctas;
   return to_status(launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+int pa_decode(const pa_kv_pool* pool, void* out, const void* q, int num_seqs, int num_q_heads,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              float scale, void* workspace, size_t workspace_bytes, int* d_status, void* stream) {
+  return pa_decode_with_ctas(pool, out, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                             context_lens, scale, 0, workspace, workspace_bytes, d_status, stream);
 }
 
 namespace {
@@ -198,12 +209,14 @@ size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int head_
          static_cast<size_t>(num_seqs) * num_q_heads * head_dim * 4;
 }
 
-int pa_decode_cascade(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
-                      int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
-                      const int32_t* context_lens, const int32_t* cu_groups,
-                      const int32_t* prefix_lens, int num_groups, float scale, void* workspace,
-                      size_t workspace_bytes, int* d_status, void* stream) {
+int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+                                int num_q_heads, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens,
+                                const int32_t* cu_groups, const int32_t* prefix_lens,
+                                int num_groups, float scale, int num_ctas, void* workspace,
+                                size_t workspace_bytes, int* d_status, void* stream) {
   pa::TraceRange trace("pa_decode_cascade");
+  if (num_ctas < 0) return PA_EINVAL;
   int rc = check_pool(pool);
   if (rc != PA_OK) return rc;
   if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_groups < 0) return PA_EINVAL;
@@ -261,7 +274,7 @@ int pa_decode_cascade(const pa_kv_pool* pool, void* out, const void* q, int num_
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.d_status = d_status;
-  a.grid_override = g_decode_ctas.load();
+  a.grid_override = num_ctas;
   if (num_groups > 0) {
     a.cu_groups = cu_groups;
     a.prefix_lens = prefix_lens;
@@ -270,6 +283,17 @@ int pa_decode_cascade(const pa_kv_pool* pool, void* out, const void* q, int num_
     a.pre_acc = pre_acc;
   }
   return to_status(launch_decode(a, st));
+}
+
+int pa_decode_cascade(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+                      int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, const int32_t* cu_groups,
+                      const int32_t* prefix_lens, int num_groups, float scale, void* workspace,
+                      size_t workspace_bytes, int* d_status, void* stream) {
+  return pa_decode_cascade_with_ctas(pool, out, q, num_seqs, num_q_heads, block_tables,
+                                     max_blocks_per_seq, context_lens, cu_groups, prefix_lens,
+                                     num_groups, scale, 0, workspace, workspace_bytes, d_status,
+                                     stream);
 }
 
 size_t pa_mixed_workspace_size(int num_seqs, int num_tokens, int num_q_heads, int head_dim,
@@ -352,7 +376,7 @@ int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.d_status = d_status;
-  a.grid_override = g_decode_ctas.load();
+  a.grid_override = 0;
   return to_status(launch_decode(a, st));
 }
 

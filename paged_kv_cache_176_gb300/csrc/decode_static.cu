@@ -16,10 +16,17 @@
 // first call before any stream capture. The call allocates nothing.
 //
 // All calls share the one array and it keeps whatever the last call left in
-// it. Nothing in it has to start at zero: every value the merge kernel reads
-// is written earlier by the same call. Calls whose work overlaps on the GPU
-// (concurrent streams, or several host threads) race on the array; run them
-// one after another.
+// it. Nothing in it has to start at zero: on every path that completes, each
+// value the merge kernel reads is written earlier by the same call. A call
+// whose status word gets PA_STATUS_TIMEOUT (a copy that never completed) may
+// leave partial slots unwritten, so its output is undefined, as for pa_decode.
+// Calls whose work overlaps on the GPU (concurrent streams, or several host
+// threads) race on the array; run them one after another.
+//
+// The cached address belongs to the CUDA context that was current when it was
+// looked up. cudaDeviceReset (or anything else that destroys the device's
+// primary context) unloads the module, so the cache is then stale: a process
+// that resets a device must not call this entry point on it again.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -67,21 +74,18 @@ int pa_decode_static_ws(const pa_kv_pool* pool, void* out, const void* q, int nu
                         int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
                         const int32_t* context_lens, float scale, int* d_status, void* stream) {
   pa::TraceRange trace("pa_decode_static_ws");
-  if (pool == nullptr) return PA_EINVAL;
-  // the sizes must fit the static scratch; the remaining checks are
-  // pa_decode's own
-  if (num_seqs > 0 && num_q_heads > 0 && pool != nullptr && pool->head_dim > 0 &&
-      max_blocks_per_seq > 0) {
-    const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, pool->head_dim,
-                                                 max_blocks_per_seq);
-    if (need > kStaticScratchBytes) return PA_EWORKSPACE;
-  }
+  // pa_decode's own argument checks first, so that a bad or unsupported call
+  // gets the same status as from pa_decode; then the size limit of the array
+  int rc = check_decode_args(pool, out, q, num_seqs, num_q_heads, block_tables,
+                             max_blocks_per_seq, context_lens);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, pool->head_dim,
+                                               max_blocks_per_seq);
+  if (need > kStaticScratchBytes) return PA_EWORKSPACE;
   void* scratch = nullptr;
-  if (num_seqs > 0) {
-    if (scratch_address(&scratch) != cudaSuccess) {
-      cudaGetLastError();
-      return PA_ECUDA;
-    }
+  if (scratch_address(&scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ECUDA;
   }
   return pa_decode(pool, out, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
                    context_lens, scale, scratch, kStaticScratchBytes, d_status, stream);

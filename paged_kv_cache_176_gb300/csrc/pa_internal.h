@@ -104,4 +104,10 @@ cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 
 int device_sm_count();
 
+// Host validation of pa_decode's arguments other than the workspace (api.cu):
+// PA_OK, or the pa_status pa_decode would return.
+int check_decode_args(const pa_kv_pool* pool, const void* out, const void* q, int num_seqs,
+                      int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens);
+
 }  // namespace pa

@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int b = 0; b < kBlocksTile; ++b) ph[b] = b < nb ? __ldg(row + b) : 0;
     return nb;
   };
-  // One producer per operand: TMA of K tiles (warp 0) or V tiles (warp 6),
+  // One producer per operand: TMA of K tiles (warp 0) or V tiles (warp 10),
   // each 128 keys = 8 pool blocks x two 64-column halves.
   auto produce = [&](const CUtensorMap* tm, int off, int stages, uint64_t* full, uint64_t* empty) {
     int ph[kBlocksTile], phn[kBlocksTile];

@@ -1,10 +1,9 @@
-// gather_probe.cu -- the measurement aid of include/pa_probe.h: stream a list
-// of pool blocks (K and V) into a ring of shared-memory stages with the decode
-// kernel's bulk copies and compute nothing.
-#include "../../include/pa_probe.h"
-#include "pa_common.cuh"
-#include "pa_internal.h"
-#include "pa_trace.h"
+// gather_probe.cu -- the measurement aid of include/pa_probe.h (libpa_probe):
+// stream a list of pool blocks (K and V) into a ring of shared-memory stages
+// with the decode kernel's bulk copies and compute nothing.
+#include "../../../include/pa_probe.h"
+#include "../pa_common.cuh"
+#include "../pa_trace.h"
 
 namespace pa {
 namespace {
@@ -77,7 +76,15 @@ extern "C" int pa_gather_probe(const pa_kv_pool* pool, const int32_t* blocks, in
   if (cudaFuncSetAttribute(pa::gather_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return PA_ECUDA;
-  const int grid = ctas > 0 ? ctas : pa::device_sm_count();
+  int grid = ctas;
+  if (grid <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&grid, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return PA_ECUDA;
+    }
+  }
   pa::gather_probe_kernel<<<grid, 256, smem, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const char*>(pool->k), static_cast<const char*>(pool->v), pool->num_blocks, blocks,
       n, stages, static_cast<int>(bytes), d_status);

@@ -247,7 +247,9 @@ def paged_workload(
 
 
 # ---------------------------------------------------------------------------
-# The five workloads. Sizes follow the pages (see the design doc for the recipe).
+# The five workloads. Sizes follow the pages: the tiny fp32 decode, the decode batch,
+# the wide-head GQA batch of the anchor model, the budgeted mixed step and
+# shared-prefix sampling.
 # ---------------------------------------------------------------------------
 
 

@@ -20,6 +20,9 @@ What pins what:
   blocks' physical IDs are scattered yet logically contiguous);
 * copy-on-write sharing equals private copies (C13-L2 page, parallel
   sampling; Inference-engine guide section 1.5);
+* the copy-on-write copy itself, on the worked parallel-sampling case: after
+  the copies and writes every reply's gathered cache is its logical token
+  sequence, and nothing else changed;
 * closed forms of softmax attention (one key, equal keys, constant values,
   zero query, a dominant logit, two keys);
 * the worked page table of the Inference-engine guide, section 1.2
@@ -377,6 +380,68 @@ def pin_kv_write(lib) -> None:
     assert np.array_equal(after[~touched].view(np.uint16), before[~touched].view(np.uint16))
 
 
+def pin_copy_on_write(lib) -> None:
+    """The copy-on-write copy, on the worked case of parallel sampling: a
+    request's 3 replies share its prompt's blocks ("C13 L2 serving", parallel
+    sampling; "Inference engine core techniques" 1.5). The 37-token prompt
+    fills blocks 0 and 1 and 5 slots of block 2. Each reply writes its first
+    token at position 37, i.e. into the shared partial block: replies 0 and 1
+    copy its 5 filled slots onto fresh blocks 7 and 9 and write there; reply 2,
+    the last holder, writes in place. Afterwards each reply's cache, gathered
+    through its table, is exactly its logical token sequence (built without a
+    pool), and every slot outside the copies and writes is unchanged."""
+    g = torch.Generator().manual_seed(11)
+    b, hkv, d, nb = 16, 2, 8, 12
+    prompt_k = torch.randn(37, hkv, d, generator=g).bfloat16()
+    prompt_v = torch.randn(37, hkv, d, generator=g).bfloat16()
+    new_k = torch.randn(3, hkv, d, generator=g).bfloat16()
+    new_v = torch.randn(3, hkv, d, generator=g).bfloat16()
+    # free blocks hold stale values of an earlier occupant; the prompt's
+    # partial block holds NaN past its 5 filled slots
+    kp = torch.randn(nb, b, hkv, d, generator=g).bfloat16()
+    vp = torch.randn(nb, b, hkv, d, generator=g).bfloat16()
+    kp[2], vp[2] = float("nan"), float("nan")
+    prompt_blocks = [4, 0, 2]  # physical blocks of logical blocks 0, 1, 2
+    for pos in range(37):
+        kp[prompt_blocks[pos // b], pos % b] = prompt_k[pos]
+        vp[prompt_blocks[pos // b], pos % b] = prompt_v[pos]
+    before = _raw(kp).copy()
+    tables = [[4, 0, 7], [4, 0, 9], [4, 0, 2]]
+    src, dst, ntok = [2, 2], [7, 9], [5, 5]
+    slots = [t[2] * b + 5 for t in tables]
+    rc = oracle.cow_write(kp, vp, new_k, new_v, torch.tensor(slots), torch.tensor(src, dtype=torch.int32),
+                          torch.tensor(dst, dtype=torch.int32), torch.tensor(ntok, dtype=torch.int32),
+                          lib=lib)
+    assert rc == 0
+    for r, table in enumerate(tables):
+        want_k = torch.cat([prompt_k, new_k[r:r + 1]])
+        want_v = torch.cat([prompt_v, new_v[r:r + 1]])
+        pos = torch.arange(38)
+        got_k = kp[torch.tensor(table)[pos // b], pos % b]
+        got_v = vp[torch.tensor(table)[pos // b], pos % b]
+        assert np.array_equal(_raw(got_k), _raw(want_k)) and np.array_equal(_raw(got_v), _raw(want_v)), r
+    touched = np.zeros((nb, b), dtype=bool)
+    for blk in dst:
+        touched[blk, :6] = True
+    touched[2, 5] = True
+    after = _raw(kp)
+    assert np.array_equal(after[~touched], before[~touched])
+    # whole-block copies: a table pointing at the copy sees the source's tokens
+    kp2, vp2 = kp.clone(), vp.clone()
+    assert oracle.copy_blocks(kp2, vp2, torch.tensor([0, 4], dtype=torch.int32),
+                              torch.tensor([11, 10], dtype=torch.int32), lib=lib) == 0
+    pos = torch.arange(37)
+    for tab in ([4, 0, 2], [10, 11, 2]):
+        got = kp2[torch.tensor(tab)[pos // b], pos % b]
+        assert np.array_equal(_raw(got), _raw(prompt_k))
+    # a pair outside the pool, or with more slots than a block holds, is skipped
+    kp3, vp3 = kp.clone(), vp.clone()
+    rc = oracle.copy_blocks(kp3, vp3, torch.tensor([1, 3], dtype=torch.int32),
+                            torch.tensor([nb, 5], dtype=torch.int32),
+                            torch.tensor([4, b + 1], dtype=torch.int32), lib=lib)
+    assert rc == 2 and np.array_equal(_raw(kp3), _raw(kp)) and np.array_equal(_raw(vp3), _raw(vp))
+
+
 ALL_PINS = [
     pin_kv_write,
     pin_page_table_example,
@@ -386,4 +451,5 @@ ALL_PINS = [
     pin_chunked_prefill,
     pin_permutation,
     pin_cow,
+    pin_copy_on_write,
 ]

@@ -11,12 +11,11 @@ from paged_kv_cache_176_gb300 import abi
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def declared_functions():
+def declared_functions(headers):
     names = []
-    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
-        if fn.endswith(".h"):
-            text = open(os.path.join(ROOT, "include", fn)).read()
-            names += re.findall(r"^PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text, flags=re.M)
+    for fn in headers:
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        names += re.findall(r"^PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text, flags=re.M)
     return names
 
 
@@ -26,10 +25,20 @@ def lib():
 
 
 def test_exports_every_declared_symbol(lib):
-    names = declared_functions()
+    """libpa exports everything pa.h and pa_serving.h declare; libpa_probe
+    everything pa_probe.h declares, and libpa none of the probes."""
+    headers = sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
+    assert "pa_probe.h" in headers
+    names = declared_functions([h for h in headers if h != "pa_probe.h"])
     assert len(names) >= 8
     for n in names:
         assert hasattr(lib, n), n
+    probe = abi.load_probe()
+    probes = declared_functions(["pa_probe.h"])
+    assert set(probes) == {"pa_gather_probe", "pa_wait_probe"}
+    for n in probes:
+        assert hasattr(probe, n), n
+        assert not hasattr(lib, n), n
 
 
 def test_version_and_strerror(lib):
@@ -99,9 +108,44 @@ def test_mixed_and_write_validation(lib):
     assert lib.pa_reshape_and_cache(ctypes.byref(pl), FAKE, FAKE, FAKE, 0, None, None) == abi.PA_OK
 
 
-def test_decode_cta_knob(lib):
-    old = abi.pa_set_decode_ctas(7)
-    assert abi.pa_set_decode_ctas(old) == 7
+def test_decode_cta_count_is_an_argument(lib):
+    """The CTA count is passed per call; the library has no setter for it."""
+    assert not hasattr(lib, "pa_set_decode_ctas")
+    pl = pool()
+    args = (ctypes.byref(pl), FAKE, FAKE, 4, 8, FAKE, 8, FAKE, 0.125)
+    assert lib.pa_decode_with_ctas(*args, -1, FAKE, 1 << 40, None, None) == abi.PA_EINVAL
+    assert lib.pa_decode_with_ctas(ctypes.byref(pool(head_dim=96)), FAKE, FAKE, 4, 8, FAKE, 8, FAKE,
+                                   0.125, 3, FAKE, 1 << 40, None, None) == abi.PA_EUNSUPPORTED
+    assert lib.pa_decode_with_ctas(*args, 3, FAKE, 16, None, None) == abi.PA_EWORKSPACE
+    bf16 = pool(dtype=1, head_dim=128)
+    assert lib.pa_decode_cascade_with_ctas(ctypes.byref(bf16), FAKE, FAKE, 4, 8, FAKE, 8, FAKE,
+                                           FAKE, FAKE, 1, 0.125, -2, FAKE, 1 << 40, None,
+                                           None) == abi.PA_EINVAL
+
+
+def test_static_workspace_checks_arguments_before_size(lib):
+    """pa_decode_static_ws returns pa_decode's status for a bad call even when
+    the batch is too large for its array; only a valid call gets PA_EWORKSPACE."""
+    S = 1 << 20
+    big = dict(S=S, hq=64)
+    f = lib.pa_decode_static_ws
+
+    def call(pl, S=4, hq=8, q=FAKE):
+        return f(ctypes.byref(pl), FAKE, q, S, hq, FAKE, 8, FAKE, 0.125, None, None)
+
+    assert call(pool(num_kv_heads=8, head_dim=256), **big) == abi.PA_EWORKSPACE
+    assert call(pool(num_kv_heads=8, head_dim=96), **big) == abi.PA_EUNSUPPORTED
+    assert call(pool(num_kv_heads=8, head_dim=256), S=S, hq=60) == abi.PA_EINVAL
+    assert call(pool(num_kv_heads=8, head_dim=256), q=None, **big) == abi.PA_EINVAL
+    assert call(pool(), S=0) == abi.PA_OK
+
+
+def test_wait_probe_validation():
+    probe = abi.load_probe()
+    assert probe.pa_wait_probe(None, 1, 1000000, None, None) == abi.PA_EINVAL
+    assert probe.pa_wait_probe(FAKE + 8, 1, 1000000, None, None) == abi.PA_EINVAL
+    assert probe.pa_wait_probe(FAKE, 1, 0, None, None) == abi.PA_EINVAL
+    assert probe.pa_wait_probe(FAKE, 1, 3 * 10**9, None, None) == abi.PA_EINVAL
 
 
 def test_binding_rejects_host_tensors():

@@ -22,14 +22,9 @@ def _bytes(t):
 
 
 def _host_apply(hk, hv, kn, vn, slots, cows):
-    for s, d, n in cows:
-        hk[d, :n] = hk[s, :n]
-        hv[d, :n] = hv[s, :n]
-    hkf, hvf = hk.view(-1, *hk.shape[2:]), hv.view(-1, *hv.shape[2:])
-    for t, slot in enumerate(slots):
-        if slot >= 0:
-            hkf[slot] = kn[t]
-            hvf[slot] = vn[t]
+    """The oracle's fused copy-on-write write on the host mirror."""
+    src, dst, ntok = (torch.tensor([c[i] for c in cows], dtype=torch.int32) for i in range(3))
+    oracle.cow_write(hk, hv, kn, vn, torch.tensor(slots, dtype=torch.int64), src, dst, ntok)
 
 
 def _i32(x):

@@ -12,7 +12,7 @@ from parity import compare, oracle_out, run_decode, to_device
 pytestmark = pytest.mark.gpu
 
 
-def run_cascade(w, cu_groups, prefix_lens, db=None):
+def run_cascade(w, cu_groups, prefix_lens, db=None, ctas=0):
     db = db or to_device(w)
     if db.slot_mapping is not None:
         pa.pa_reshape_and_cache(db.k_pool, db.v_pool, db.k_new, db.v_new, db.slot_mapping,
@@ -20,16 +20,10 @@ def run_cascade(w, cu_groups, prefix_lens, db=None):
     out = torch.empty_like(db.q)
     cu = torch.tensor(cu_groups, dtype=torch.int32, device="cuda")
     pl = torch.tensor(prefix_lens, dtype=torch.int32, device="cuda")
-    pa.pa_decode_cascade(out, db.q, db.k_pool, db.v_pool, db.block_tables, db.context_lens, cu, pl,
-                         w.scale, d_status=db.status)
+    pa.pa_decode_cascade_with_ctas(out, db.q, db.k_pool, db.v_pool, db.block_tables,
+                                   db.context_lens, cu, pl, w.scale, ctas, d_status=db.status)
     torch.cuda.synchronize()
     return out, db
-
-
-@pytest.fixture(autouse=True)
-def default_grid():
-    yield
-    pa.pa_set_decode_ctas(0)
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (16, 4), (32, 4), (64, 8)])
@@ -47,8 +41,7 @@ def test_cascade_groups_and_edges(hq, hkv, ctas):
                          torch.bfloat16, write_new=False)
     cu, pl = [0, 70, 71, 72, 74], [400, 208, 0, 400]
     w = W.share_prefix(w, cu, pl)
-    pa.pa_set_decode_ctas(ctas)
-    out, db = run_cascade(w, cu, pl)
+    out, db = run_cascade(w, cu, pl, ctas=ctas)
     assert int(db.status.item()) == 0
     compare(out, oracle_out(w), torch.bfloat16)
 

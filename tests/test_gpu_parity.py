@@ -13,13 +13,6 @@ from parity import compare, oracle_out, run_decode, run_mixed, to_device
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True)
-def _default_ctas():
-    old = pa.pa_set_decode_ctas(0)
-    yield
-    pa.pa_set_decode_ctas(old)
-
-
 def _bytes(t: torch.Tensor) -> np.ndarray:
     t = t.contiguous().cpu()
     if t.dtype == torch.bfloat16:
@@ -95,8 +88,7 @@ def test_decode_split_counts(ctas, hkv):
     heads take the tensor-core products, 4 the CUDA-core ones."""
     w = W.paged_workload("split", 5, [1, 15, 16, 17, 33, 100, 257, 600], [1] * 8, 4 * hkv, hkv, 128,
                          200, torch.bfloat16, write_new=True)
-    pa.pa_set_decode_ctas(ctas)
-    out, db = run_decode(w)
+    out, db = run_decode(w, ctas=ctas)
     compare(out, oracle_out(w), torch.bfloat16)
     assert int(db.status.item()) == 0
 
@@ -108,11 +100,7 @@ def test_decode_cta_range_beyond_table_cache(dtype):
     fp32 with 8 KV heads moves half blocks (two units per block)."""
     w = W.paged_workload("long", 13, [9000, 8000], [1, 1], 32, 8, 128, 1300, dtype,
                          write_new=True)
-    pa.pa_set_decode_ctas(1)
-    try:
-        out, db = run_decode(w)
-    finally:
-        pa.pa_set_decode_ctas(0)
+    out, db = run_decode(w, ctas=1)
     compare(out, oracle_out(w), dtype)
     assert int(db.status.item()) == 0
 
@@ -128,8 +116,7 @@ def test_decode_shapes(d, hq, hkv, dtype):
     w = W.paged_workload("shape", 11, [3, 16, 31, 200, 513], [1] * 5, hq, hkv, d, 128, dtype,
                          write_new=True)
     for ctas in (0, 5):
-        pa.pa_set_decode_ctas(ctas)
-        out, _ = run_decode(w)
+        out, _ = run_decode(w, ctas=ctas)
         compare(out, oracle_out(w), dtype)
 
 
@@ -246,6 +233,9 @@ def test_mixed_step_scaled_full():
 
 
 def test_mixed_step_full_sampled():
+    """The full mixed step (budget 2048: 128 decode rows + chunks 512/512/512/384
+    of 32,768-token prompts, 64/8 heads): every decode row and 64 sampled rows
+    per prefill chunk (all heads) against the oracle."""
     w = W.mixed_step()
     out, db = run_mixed(w)
     assert int(db.status.item()) == 0
@@ -255,9 +245,12 @@ def test_mixed_step_full_sampled():
     mask[:nd] = 1
     cu = w.cu_q_lens.tolist()
     for s in range(nd, w.num_seqs):
-        rows = rng.choice(np.arange(cu[s], cu[s + 1]), size=8, replace=False)
+        # 64 seeded rows of every chunk, plus its first and last rows (the
+        # shortest and the longest key ranges)
+        rows = rng.choice(np.arange(cu[s], cu[s + 1]), size=64, replace=False)
         mask[rows] = 1
-        mask[cu[s + 1] - 1] = 1  # last row of each chunk (longest key range)
+        mask[cu[s]] = 1
+        mask[cu[s + 1] - 1] = 1
     ref = oracle_out(w, row_mask=mask)
     compare(out, ref, torch.bfloat16, rows=np.nonzero(mask)[0])
 

@@ -37,10 +37,10 @@ def drive_with_oracle(loop, num_blocks, num_reqs, dtype, on_step=None):
             break
         torch.cuda.synchronize()
         S, T = p.num_seqs, p.num_tokens
-        for i in range(p.num_cow):
-            n = int(p.cow_ntok[i])
-            hk[int(p.cow_dst[i]), :n] = hk[int(p.cow_src[i]), :n]
-            hv[int(p.cow_dst[i]), :n] = hv[int(p.cow_src[i]), :n]
+        if p.num_cow:
+            assert oracle.copy_blocks(hk, hv, torch.from_numpy(p.cow_src[:p.num_cow].copy()),
+                                      torch.from_numpy(p.cow_dst[:p.num_cow].copy()),
+                                      torch.from_numpy(p.cow_ntok[:p.num_cow].copy())) == 0
         oracle.reshape_and_cache(hk, hv, loop.k_new[:T].cpu(), loop.v_new[:T].cpu(),
                                  torch.from_numpy(p.slot_mapping[:T].copy()))
         ref = oracle.paged_attention(loop.q[:T].cpu(), hk, hv,
@@ -122,7 +122,5 @@ def test_copy_blocks_bit_exact():
     dk, dv = k.cuda(), v.cuda()
     pa_copy_blocks(dk, dv, src.cuda(), dst.cuda())
     torch.cuda.synchronize()
-    for s, d_ in zip(src.tolist(), dst.tolist()):
-        k[d_] = k[s]
-        v[d_] = v[s]
+    assert oracle.copy_blocks(k, v, src, dst) == 0
     assert np.array_equal(_bytes(dk), _bytes(k)) and np.array_equal(_bytes(dv), _bytes(v))

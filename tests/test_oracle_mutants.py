@@ -43,6 +43,14 @@ MUTANTS = {
     # KV write lands one slot late
     "write_offset": [("int64_t offset = slot % block_size;",
                       "int64_t offset = (slot + 1) % block_size;")],
+    # copy-on-write copies one filled slot too few
+    "cow_slot_short": [("int slots = ntok ? ntok[i] : block_size;",
+                        "int slots = ntok ? ntok[i] - 1 : block_size;")],
+    # copy-on-write copies the whole block, unfilled slots included
+    "cow_whole_block": [("int slots = ntok ? ntok[i] : block_size;", "int slots = block_size;")],
+    # copy direction reversed (the copy overwrites the shared block)
+    "cow_reversed": [("memcpy((char*)k_pool + to * block_bytes, (const char*)k_pool + from * block_bytes, bytes);",
+                      "memcpy((char*)k_pool + from * block_bytes, (const char*)k_pool + to * block_bytes, bytes);")],
 }
 
 
