@@ -12,8 +12,9 @@
  * ---------------------------------------
  *  - Pointers marked "device" are CUDA device pointers owned by the caller; the
  *    library allocates no memory and keeps no state between calls that could
- *    change a result (it caches only per-device facts: the SM count, and the
- *    address of pa_decode_static_ws's array).
+ *    change a result (it caches only per-device facts: the SM count, the
+ *    address of pa_decode_static_ws's array, and pa_decode_cascade's
+ *    auxiliary stream and events).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream). PA_OK means "validated and enqueued".
  *  - Host-side validation looks only at scalars and pointer values; on any
@@ -190,11 +191,16 @@ PA_API int pa_decode_static_ws(const pa_kv_pool* pool, void* out, const void* q,
  * guarantees the equality (it is not checked). Sequences outside every group,
  * and groups with prefix_lens[g] == 0, are plain decode.
  *
- * Steps, all on the caller's stream: (1) one tensor-core pass per group and
- * KV head computes the partials of every member's query rows against the
- * shared prefix (a dense contraction: members x heads rows by prefix keys);
- * (2) the decode kernels walk each sequence's remaining blocks and merge the
- * prefix partial in.
+ * Steps: (1) one tensor-core pass per group and KV head computes the
+ * partials of every member's query rows against the shared prefix (a dense
+ * contraction: members x heads rows by prefix keys); (2) the decode kernel
+ * walks each sequence's remaining blocks; (3) a merge kernel folds the prefix
+ * partials in. (1) and (2) run side by side: (2) on the caller's stream with
+ * all but 36 SMs, (1) on an auxiliary stream of the library's own (one per
+ * device, created at the first call with that device current and kept until
+ * the process exits), forked from the caller's stream with an event and
+ * joined back before (3). The library serializes cascade calls around that
+ * stream and its two events. With num_groups == 0 the call is pa_decode.
  *
  *  cu_groups     device int32 [num_groups + 1], non-decreasing, within [0, num_seqs]
  *  prefix_lens   device int32 [num_groups], tokens; multiple of 16

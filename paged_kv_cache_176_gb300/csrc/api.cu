@@ -4,6 +4,7 @@
 // happen in the kernels (see pa.h).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -200,6 +201,45 @@ size_t cascade_acc_offset(int num_seqs, int num_q_heads, int head_dim) {
   return cascade_ml_offset(num_seqs, num_q_heads, head_dim) +
          align_up_sz(static_cast<size_t>(num_seqs) * num_q_heads * 8, 256);
 }
+
+// The cascade runs its prefix pass and its suffix decode side by side: the
+// decode kernel streams the suffixes from HBM on all but kCascadePrefixSms
+// SMs, and the prefix pass (tensor cores, short and latency-bound) fills the
+// SMs left free. A per-device auxiliary stream and two events (created on
+// first use, kept for the life of the process) fork the prefix pass off the
+// caller's stream and join it back before the merge; the library serializes
+// cascade calls around them.
+constexpr int kCascadePrefixSms = 36;
+struct CascadeStreams {
+  cudaStream_t aux = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_cascade_mu;
+std::vector<CascadeStreams> g_cascade_streams;
+
+// Caller holds g_cascade_mu.
+cudaError_t cascade_streams(CascadeStreams** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (static_cast<int>(g_cascade_streams.size()) <= dev) g_cascade_streams.resize(dev + 1);
+  CascadeStreams& c = g_cascade_streams[dev];
+  if (c.aux == nullptr) {
+    CascadeStreams n;
+    err = cudaStreamCreateWithFlags(&n.aux, cudaStreamNonBlocking);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming);
+    if (err != cudaSuccess) {
+      if (n.join) cudaEventDestroy(n.join);
+      if (n.fork) cudaEventDestroy(n.fork);
+      if (n.aux) cudaStreamDestroy(n.aux);
+      return err;
+    }
+    c = n;
+  }
+  *out = &c;
+  return cudaSuccess;
+}
 }  // namespace
 
 size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int head_dim,
@@ -238,27 +278,6 @@ int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q
   char* ws = static_cast<char*>(workspace);
   void* pre_ml = ws + cascade_ml_offset(num_seqs, num_q_heads, pool->head_dim);
   void* pre_acc = ws + cascade_acc_offset(num_seqs, num_q_heads, pool->head_dim);
-  if (num_groups > 0) {
-    // 1. every group's decode rows against its shared prefix, once, on the tensor cores
-    PrefillArgs pf = {};
-    pf.pool = view(pool);
-    pf.q = q;
-    pf.cu_q_lens = cu_groups;
-    pf.num_seqs = num_groups;
-    pf.num_tokens = num_seqs;
-    pf.num_q_heads = num_q_heads;
-    pf.block_tables = block_tables;
-    pf.max_blocks_per_seq = max_blocks_per_seq;
-    pf.context_lens = prefix_lens;
-    pf.scale = scale;
-    pf.d_status = d_status;
-    pf.prefix_mode = 1;
-    pf.pre_ml = pre_ml;
-    pf.pre_acc = pre_acc;
-    rc = to_status(launch_prefix_partials(pf, st));
-    if (rc != PA_OK) return rc;
-  }
-  // 2. every sequence's own blocks after its prefix, merged with the prefix partial
   DecodeArgs a = {};
   a.pool = view(pool);
   a.out = out;
@@ -275,13 +294,50 @@ int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q
   a.workspace_bytes = workspace_bytes;
   a.d_status = d_status;
   a.grid_override = num_ctas;
-  if (num_groups > 0) {
-    a.cu_groups = cu_groups;
-    a.prefix_lens = prefix_lens;
-    a.num_groups = num_groups;
-    a.pre_ml = pre_ml;
-    a.pre_acc = pre_acc;
-  }
+  if (num_groups == 0) return to_status(launch_decode(a, st));
+  a.cu_groups = cu_groups;
+  a.prefix_lens = prefix_lens;
+  a.num_groups = num_groups;
+  a.pre_ml = pre_ml;
+  a.pre_acc = pre_acc;
+  a.defer_prefix = 1;
+  if (num_ctas == 0) a.grid_override = std::max(1, device_sm_count() - kCascadePrefixSms);
+  // every group's decode rows against its shared prefix, once, on the tensor cores
+  PrefillArgs pf = {};
+  pf.pool = view(pool);
+  pf.q = q;
+  pf.cu_q_lens = cu_groups;
+  pf.num_seqs = num_groups;
+  pf.num_tokens = num_seqs;
+  pf.num_q_heads = num_q_heads;
+  pf.block_tables = block_tables;
+  pf.max_blocks_per_seq = max_blocks_per_seq;
+  pf.context_lens = prefix_lens;
+  pf.scale = scale;
+  pf.d_status = d_status;
+  pf.prefix_mode = 1;
+  pf.pre_ml = pre_ml;
+  pf.pre_acc = pre_acc;
+  // fork: the suffix decode on the caller's stream (launched first, so it
+  // takes its SMs first), the prefix pass on the auxiliary stream; join; merge
+  std::lock_guard<std::mutex> lock(g_cascade_mu);
+  CascadeStreams* cs = nullptr;
+  rc = to_status(cascade_streams(&cs));
+  if (rc != PA_OK) return rc;
+  rc = to_status(cudaEventRecord(cs->fork, st));
+  if (rc == PA_OK) rc = to_status(cudaStreamWaitEvent(cs->aux, cs->fork, 0));
+  if (rc != PA_OK) return rc;
+  a.launch_part = 1;
+  rc = to_status(launch_decode(a, st));
+  if (rc != PA_OK) return rc;
+  rc = to_status(launch_prefix_partials(pf, cs->aux));
+  // join even when the prefix launch failed, so the auxiliary stream never
+  // runs ahead of later work on the caller's stream
+  const int rc_join = to_status(cudaEventRecord(cs->join, cs->aux));
+  const int rc_wait = rc_join == PA_OK ? to_status(cudaStreamWaitEvent(st, cs->join, 0)) : rc_join;
+  if (rc != PA_OK) return rc;
+  if (rc_wait != PA_OK) return rc_wait;
+  a.launch_part = 2;
   return to_status(launch_decode(a, st));
 }
 

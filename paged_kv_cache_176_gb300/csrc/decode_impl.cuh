@@ -209,6 +209,10 @@ struct DecodeParams {
   int num_groups;
   const float2* pre_ml;  // [num_seqs, hq]
   const float* pre_acc;  // [num_seqs, hq, D]
+  // the prefix partials are computed concurrently (another stream): the
+  // decode kernel leaves every cascade sequence as a partial and only the
+  // merge kernel, ordered after both, folds the prefix in
+  int defer_prefix;
   // tensor-core path: the K and V pools as 4-D maps (see make_tmap_pool_heads)
   CUtensorMap tm_k;
   CUtensorMap tm_v;
@@ -598,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         if (hr >= G) continue;
         const int head = g * G + hr;
         float mr = r ? m1 : m0, lr_ = r ? l1 : l0;
-        if (whole) {
+        if (whole && !(has_pre && p.defer_prefix)) {
           bool pre_poisoned = false;
           if (has_pre) {
             // fold in the shared-prefix partial of this sequence
@@ -1007,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     // 3. write: the final row when this CTA saw the whole sequence, else a partial
     if (sub == 0 && tg == 0) {
-      if (whole) {
+      if (whole && !(has_pre && p.defer_prefix)) {
         T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(row) * p.hq + head0) * D;
         bool pre_poisoned[C::kGL];
 #pragma unroll
@@ -1101,7 +1105,9 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
   if (a1 > a0) {
     c_first = ((a0 + 1) * grid - 1) / B;
     c_last = (a1 * grid - 1) / B;
-    if (c_first == c_last) return;  // finished by the decode kernel
+    // one CTA saw the whole sequence: it wrote the final row, unless the
+    // prefix fold was left to this kernel
+    if (c_first == c_last && !p.defer_prefix) return;
   } else if (p.cu_groups == nullptr) {
     return;  // not a decode sequence, or zeroed by the decode kernel
   }
@@ -1114,6 +1120,7 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
     }
     has_pre = prefix_blocks(p, s, p.context_lens[s], &bad) > 0;
     if (a1 <= a0 && !has_pre) return;
+    if (a1 > a0 && c_first == c_last && !has_pre) return;  // finished by the decode kernel
   }
   float m = -INFINITY, l = 0.f;
   float acc[kPer];
@@ -1215,6 +1222,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   p.num_groups = a.num_groups;
   p.pre_ml = static_cast<const float2*>(a.pre_ml);
   p.pre_acc = static_cast<const float*>(a.pre_acc);
+  p.defer_prefix = a.defer_prefix;
   if constexpr (Cfg<T, D, G, WH>::kMma) {
     if (!make_tmap_pool_heads(&p.tm_k, a.pool.k, D, hkv, static_cast<uint64_t>(a.pool.num_blocks)) ||
         !make_tmap_pool_heads(&p.tm_v, a.pool.v, D, hkv, static_cast<uint64_t>(a.pool.num_blocks)))
@@ -1222,14 +1230,19 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   }
 
   auto kern = decode_kernel<T, D, G, WH>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-  if (err != cudaSuccess) return err;
-  kern<<<grid, kThreads, L.total, stream>>>(p);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  if (a.launch_part != 2) {
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, kThreads, L.total, stream>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  if (a.launch_part == 1) return cudaSuccess;  // the caller launches the merge later
 
   // merge kernel, launched with programmatic stream serialization so its
-  // launch overlaps the decode kernel's tail (it waits with griddepcontrol.wait)
+  // launch overlaps the decode kernel's tail (it waits with griddepcontrol.wait);
+  // launched on its own (after a join of streams) it needs no such overlap
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.num_seqs * a.num_q_heads + 7) / 8);
   cfg.blockDim = dim3(256);
@@ -1239,7 +1252,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.launch_part == 2 ? 0 : 1;
   return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<T, D>, p, grid);
 }
 

@@ -61,6 +61,8 @@ struct DecodeArgs {
   int num_groups;
   const void* pre_ml;
   const void* pre_acc;
+  int defer_prefix;  // 1: the prefix partials are written concurrently; only the merge folds them
+  int launch_part;   // 0: decode kernel and merge; 1: the decode kernel only; 2: the merge only
 };
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim);
 // per (dtype, head_dim) entry points, one translation unit each
