@@ -12,9 +12,8 @@
  * ---------------------------------------
  *  - Pointers marked "device" are CUDA device pointers owned by the caller; the
  *    library allocates no memory and keeps no state between calls that could
- *    change a result (it caches only per-device facts: the SM count, the
- *    address of pa_decode_static_ws's array, and pa_decode_cascade's
- *    auxiliary stream and events).
+ *    change a result (it caches only per-device facts: the SM count, and the
+ *    address of pa_decode_static_ws's array).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream). PA_OK means "validated and enqueued".
  *  - Host-side validation looks only at scalars and pointer values; on any
@@ -195,12 +194,11 @@ PA_API int pa_decode_static_ws(const pa_kv_pool* pool, void* out, const void* q,
  * partials of every member's query rows against the shared prefix (a dense
  * contraction: members x heads rows by prefix keys); (2) the decode kernel
  * walks each sequence's remaining blocks; (3) a merge kernel folds the prefix
- * partials in. (1) and (2) run side by side: (2) on the caller's stream with
- * all but 36 SMs, (1) on an auxiliary stream of the library's own (one per
- * device, created at the first call with that device current and kept until
- * the process exits), forked from the caller's stream with an event and
- * joined back before (3). The library serializes cascade calls around that
- * stream and its two events. With num_groups == 0 the call is pa_decode.
+ * partials in. All three run on the caller's stream, (1) and (2) side by
+ * side: (2) is launched first on all but 36 SMs, (1) right after it as a
+ * programmatic dependent launch that takes the SMs (2) leaves free (neither
+ * waits for the other), and (3) after both. With num_groups == 0 the call is
+ * pa_decode.
  *
  *  cu_groups     device int32 [num_groups + 1], non-decreasing, within [0, num_seqs]
  *  prefix_lens   device int32 [num_groups], tokens; multiple of 16
@@ -256,7 +254,12 @@ PA_API size_t pa_mixed_workspace_size(int num_seqs, int num_tokens, int num_q_he
  * 0 .. that position (causal over absolute positions, as in the glossary
  * page's chunked-prefill example). q_len == 1 rows take the decode kernel;
  * q_len > 1 rows take the prefill kernel (tcgen05 tensor cores for bf16). The
- * result equals one-pass causal prefill for any chunk split.
+ * result equals one-pass causal prefill for any chunk split. When the step
+ * holds at least 1024 prefill tokens (num_tokens - num_seqs >= 1024) on the
+ * tensor-core path, the decode rows run on 48 SMs and the prefill beside
+ * them on the other SMs (a programmatic dependent launch on the same stream;
+ * neither kernel waits for the other); otherwise the prefill runs first on
+ * all SMs, then the decode.
  *
  *  cu_q_lens     device int32 [num_seqs + 1], cu_q_lens[0] = 0, non-decreasing,
  *                cu_q_lens[num_seqs] = num_tokens

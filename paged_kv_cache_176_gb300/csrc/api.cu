@@ -202,44 +202,22 @@ size_t cascade_acc_offset(int num_seqs, int num_q_heads, int head_dim) {
          align_up_sz(static_cast<size_t>(num_seqs) * num_q_heads * 8, 256);
 }
 
-// The cascade runs its prefix pass and its suffix decode side by side: the
-// decode kernel streams the suffixes from HBM on all but kCascadePrefixSms
-// SMs, and the prefix pass (tensor cores, short and latency-bound) fills the
-// SMs left free. A per-device auxiliary stream and two events (created on
-// first use, kept for the life of the process) fork the prefix pass off the
-// caller's stream and join it back before the merge; the library serializes
-// cascade calls around them.
+// Decode beside prefill: the decode kernel (HBM-bound) runs on a reduced set
+// of persistent CTAs, and the tensor-core prefill or prefix kernel, launched
+// right after it on the same stream as a programmatic dependent, takes the
+// SMs it leaves free (it may start once every decode CTA has staged its
+// blocks, and neither kernel waits for the other); the merge kernel, an
+// ordinary launch, runs after both. On fewer SMs the decode no longer
+// saturates HBM, so each of its SMs streams more bytes, and an SM a decode
+// CTA leaves goes to the prefill.
+//  - cascade decode: the decode streams the suffixes on all but
+//    kCascadePrefixSms SMs beside the (short, latency-bound) prefix pass;
+//  - mixed step: the decode takes kMixedDecodeSms SMs beside a prefill of at
+//    least kMixedPrefillTokens tokens (a bound the host can see:
+//    num_tokens - num_seqs); smaller prefills run after the decode on all SMs.
 constexpr int kCascadePrefixSms = 36;
-struct CascadeStreams {
-  cudaStream_t aux = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-std::mutex g_cascade_mu;
-std::vector<CascadeStreams> g_cascade_streams;
-
-// Caller holds g_cascade_mu.
-cudaError_t cascade_streams(CascadeStreams** out) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (static_cast<int>(g_cascade_streams.size()) <= dev) g_cascade_streams.resize(dev + 1);
-  CascadeStreams& c = g_cascade_streams[dev];
-  if (c.aux == nullptr) {
-    CascadeStreams n;
-    err = cudaStreamCreateWithFlags(&n.aux, cudaStreamNonBlocking);
-    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming);
-    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming);
-    if (err != cudaSuccess) {
-      if (n.join) cudaEventDestroy(n.join);
-      if (n.fork) cudaEventDestroy(n.fork);
-      if (n.aux) cudaStreamDestroy(n.aux);
-      return err;
-    }
-    c = n;
-  }
-  *out = &c;
-  return cudaSuccess;
-}
+constexpr int kMixedDecodeSms = 48;
+constexpr int kMixedPrefillTokens = 1024;
 }  // namespace
 
 size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int head_dim,
@@ -318,25 +296,14 @@ int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q
   pf.prefix_mode = 1;
   pf.pre_ml = pre_ml;
   pf.pre_acc = pre_acc;
-  // fork: the suffix decode on the caller's stream (launched first, so it
-  // takes its SMs first), the prefix pass on the auxiliary stream; join; merge
-  std::lock_guard<std::mutex> lock(g_cascade_mu);
-  CascadeStreams* cs = nullptr;
-  rc = to_status(cascade_streams(&cs));
-  if (rc != PA_OK) return rc;
-  rc = to_status(cudaEventRecord(cs->fork, st));
-  if (rc == PA_OK) rc = to_status(cudaStreamWaitEvent(cs->aux, cs->fork, 0));
-  if (rc != PA_OK) return rc;
+  pf.beside_previous = 1;
+  // the suffix decode first (it takes its SMs), the prefix pass beside it,
+  // then the merge, which folds the prefix partials in, after both
   a.launch_part = 1;
   rc = to_status(launch_decode(a, st));
   if (rc != PA_OK) return rc;
-  rc = to_status(launch_prefix_partials(pf, cs->aux));
-  // join even when the prefix launch failed, so the auxiliary stream never
-  // runs ahead of later work on the caller's stream
-  const int rc_join = to_status(cudaEventRecord(cs->join, cs->aux));
-  const int rc_wait = rc_join == PA_OK ? to_status(cudaStreamWaitEvent(st, cs->join, 0)) : rc_join;
+  rc = to_status(launch_prefix_partials(pf, st));
   if (rc != PA_OK) return rc;
-  if (rc_wait != PA_OK) return rc_wait;
   a.launch_part = 2;
   return to_status(launch_decode(a, st));
 }
@@ -415,8 +382,6 @@ int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_
   pf.context_lens = context_lens;
   pf.scale = scale;
   pf.d_status = d_status;
-  rc = to_status(launch_prefill(pf, st));
-  if (rc != PA_OK) return rc;
   DecodeArgs a = {};
   a.pool = view(pool);
   a.out = out;
@@ -433,6 +398,22 @@ int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_
   a.workspace_bytes = workspace_bytes;
   a.d_status = d_status;
   a.grid_override = 0;
+  // prefill rows are at least num_tokens - num_seqs (every sequence that is
+  // not a decode row contributes two or more)
+  if (num_tokens - num_seqs >= kMixedPrefillTokens && prefill_on_tensor_cores(pf)) {
+    // decode on kMixedDecodeSms CTAs, the prefill beside it, then the merge
+    a.grid_override = std::min(kMixedDecodeSms, device_sm_count());
+    a.launch_part = 1;
+    rc = to_status(launch_decode(a, st));
+    if (rc != PA_OK) return rc;
+    pf.beside_previous = 1;
+    rc = to_status(launch_prefill(pf, st));
+    if (rc != PA_OK) return rc;
+    a.launch_part = 2;
+    return to_status(launch_decode(a, st));
+  }
+  rc = to_status(launch_prefill(pf, st));
+  if (rc != PA_OK) return rc;
   return to_status(launch_decode(a, st));
 }
 

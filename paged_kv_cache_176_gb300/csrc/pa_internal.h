@@ -96,12 +96,19 @@ struct PrefillArgs {
   int prefix_mode;
   void* pre_ml;
   void* pre_acc;
+  // 1: launched as a programmatic dependent of the kernel before it on the
+  // stream (a decode kernel that signals early), so that it runs beside that
+  // kernel on the SMs it leaves free; the prefill reads nothing that kernel
+  // writes and never waits for it
+  int beside_previous;
 };
 bool prefill_supported(int dtype, int head_dim, int group);
 // the tensor-core kernel in prefix mode (bf16, head_dim 128)
 bool prefix_supported(int dtype, int head_dim, int group, int num_groups);
 cudaError_t launch_prefix_partials(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+// true when launch_prefill takes the tensor-core kernel for these arguments
+bool prefill_on_tensor_cores(const PrefillArgs& a);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 
 int device_sm_count();

@@ -579,7 +579,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   cudaError_t err =
       cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  prefill_tc_kernel<<<dim3(tiles, hkv), kThreadsTc, smem, stream>>>(tq, tk, tv, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles, hkv);
+  cfg.blockDim = dim3(kThreadsTc);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.beside_previous ? 1 : 0;
+  err = cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tq, tk, tv, p);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -601,6 +612,8 @@ bool prefill_supported(int dtype, int head_dim, int group) {
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return false;
   return group == 1 || group == 2 || group == 4 || group == 8;
 }
+
+bool prefill_on_tensor_cores(const PrefillArgs& a) { return tc_supported(a); }
 
 // bf16 with head_dim 128 runs on the tensor cores; the other shapes and fp32
 // run on the CUDA-core kernel (prefill_simt.cu).
