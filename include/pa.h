@@ -255,11 +255,11 @@ PA_API size_t pa_mixed_workspace_size(int num_seqs, int num_tokens, int num_q_he
  * page's chunked-prefill example). q_len == 1 rows take the decode kernel;
  * q_len > 1 rows take the prefill kernel (tcgen05 tensor cores for bf16). The
  * result equals one-pass causal prefill for any chunk split. When the step
- * holds at least 1024 prefill tokens (num_tokens - num_seqs >= 1024) on the
- * tensor-core path, the decode rows run on 48 SMs and the prefill beside
- * them on the other SMs (a programmatic dependent launch on the same stream;
- * neither kernel waits for the other); otherwise the prefill runs first on
- * all SMs, then the decode.
+ * is dominated by prefill on the tensor-core path (with P = num_tokens -
+ * num_seqs: P >= 1024 and num_seqs <= P / 12), the decode rows run on 48 SMs
+ * and the prefill beside them on the other SMs (a programmatic dependent
+ * launch on the same stream; neither kernel waits for the other); otherwise
+ * the prefill runs first on all SMs, then the decode.
  *
  *  cu_q_lens     device int32 [num_seqs + 1], cu_q_lens[0] = 0, non-decreasing,
  *                cu_q_lens[num_seqs] = num_tokens

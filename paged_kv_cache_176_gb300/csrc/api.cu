@@ -212,12 +212,19 @@ size_t cascade_acc_offset(int num_seqs, int num_q_heads, int head_dim) {
 // CTA leaves goes to the prefill.
 //  - cascade decode: the decode streams the suffixes on all but
 //    kCascadePrefixSms SMs beside the (short, latency-bound) prefix pass;
-//  - mixed step: the decode takes kMixedDecodeSms SMs beside a prefill of at
-//    least kMixedPrefillTokens tokens (a bound the host can see:
-//    num_tokens - num_seqs); smaller prefills run after the decode on all SMs.
+//  - mixed step: the decode takes kMixedDecodeSms SMs beside the prefill when
+//    the prefill dominates the step. The host sees only counts: prefill
+//    tokens P >= num_tokens - num_seqs, decode rows D <= num_seqs. A decode
+//    row reads its whole context (a few to tens of MB), a prefill token costs
+//    tensor work in proportion to its context, so the split is taken only
+//    for P >= kMixedPrefillTokens and num_seqs <= P / kMixedTokensPerSeq
+//    (a step of long prefill chunks and few decode rows); a decode-heavy
+//    step (hundreds of decode rows beside short chunks) runs the prefill,
+//    then the decode on all SMs.
 constexpr int kCascadePrefixSms = 36;
 constexpr int kMixedDecodeSms = 48;
 constexpr int kMixedPrefillTokens = 1024;
+constexpr int kMixedTokensPerSeq = 12;
 }  // namespace
 
 size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int head_dim,
@@ -400,7 +407,9 @@ int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_
   a.grid_override = 0;
   // prefill rows are at least num_tokens - num_seqs (every sequence that is
   // not a decode row contributes two or more)
-  if (num_tokens - num_seqs >= kMixedPrefillTokens && prefill_on_tensor_cores(pf)) {
+  const int prefill_min = num_tokens - num_seqs;
+  if (prefill_min >= kMixedPrefillTokens && num_seqs * kMixedTokensPerSeq <= prefill_min &&
+      prefill_on_tensor_cores(pf)) {
     // decode on kMixedDecodeSms CTAs, the prefill beside it, then the merge
     a.grid_override = std::min(kMixedDecodeSms, device_sm_count());
     a.launch_part = 1;
