@@ -1097,6 +1097,22 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
   if (item >= p.num_seqs * p.hq) return;
   const int s = item / p.hq, h = item % p.hq;
   const int lane = threadIdx.x & 31;
+  // cascade decode: this row's prefix partial, loaded first (its address
+  // depends on nothing else, and in-bounds for every row) so that its latency
+  // overlaps the lookups below; used only when the row has a prefix
+  float2 pml = make_float2(-INFINITY, 0.f);
+  float pacc[kPer];
+  if (p.cu_groups != nullptr) {
+    const int64_t idx = static_cast<int64_t>(s) * p.hq + h;
+    pml = p.pre_ml[idx];
+    const float* src = p.pre_acc + idx * D + lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2) {
+      const float2 x = *reinterpret_cast<const float2*>(src + e);
+      pacc[e] = x.x;
+      pacc[e + 1] = x.y;
+    }
+  }
   const int* prefix = p.ws_prefix;
   const int64_t B = prefix[p.num_seqs];
   const int64_t a0 = prefix[s], a1 = prefix[s + 1];
@@ -1161,15 +1177,12 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
     }
   }
   if (has_pre) {
-    const int64_t idx = static_cast<int64_t>(s) * p.hq + h;
-    const float2 pml = p.pre_ml[idx];
-    const float* src = p.pre_acc + idx * D + lane * kPer;
     poisoned |= pml.y < 0.f;
     const float mn = fmaxf(m, pml.x);
     const float a = merge_factor(m, mn), b = merge_factor(pml.x, mn);
     l = l * a + pml.y * b;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = acc[e] * a + src[e] * b;
+    for (int e = 0; e < kPer; ++e) acc[e] = acc[e] * a + pacc[e] * b;
   }
   const float inv = poisoned ? 0.f : 1.f / l;
   T* dst = static_cast<T*>(p.out) + (static_cast<int64_t>(query_row(p, s)) * p.hq + h) * D + lane * kPer;
