@@ -277,6 +277,27 @@ PA_API int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const
                   const int64_t* slot_mapping, void* workspace, size_t workspace_bytes,
                   int* d_status, void* stream);
 
+/*
+ * pa_mixed_step with the size of the tensor-core prefill units fixed:
+ * prefill_q_tiles = 1 or 2 query tiles of 128 rows per unit (0: the library
+ * chooses from the sizes, as pa_mixed_step does; other values return
+ * PA_EINVAL). Two-tile units share each K/V tile between both tiles and
+ * overlap one tile's softmax with the other's products; one-tile units give
+ * twice as many units for small steps. Both compute the same attention; a
+ * row's last bits can differ between them where a tile's first row decides
+ * whether the row's exponents take the masked form. For tuning and for tests
+ * that run both unit shapes on the same inputs; an argument, never library
+ * state.
+ */
+PA_API int pa_mixed_step_with_units(const pa_kv_pool* pool, void* out, const void* q,
+                                    const int32_t* cu_q_lens, int num_seqs, int num_tokens,
+                                    int num_q_heads, const int32_t* context_lens,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    float scale, int token_budget, const void* k_new,
+                                    const void* v_new, const int64_t* slot_mapping,
+                                    int prefill_q_tiles, void* workspace, size_t workspace_bytes,
+                                    int* d_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

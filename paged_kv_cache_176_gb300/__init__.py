@@ -13,6 +13,7 @@ from .abi import (  # noqa: F401
     pa_mixed_workspace_size,
     pa_reshape_and_cache,
     pa_decode_with_ctas,
+    pa_mixed_step_with_units,
     pa_decode_cascade_with_ctas,
     pa_strerror,
     pa_version,
@@ -27,6 +28,7 @@ __all__ = [
     "pa_mixed_step",
     "pa_mixed_workspace_size",
     "pa_decode_with_ctas",
+    "pa_mixed_step_with_units",
     "pa_decode_cascade_with_ctas",
     "pa_strerror",
     "pa_version",

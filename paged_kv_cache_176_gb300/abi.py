@@ -81,6 +81,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_mixed_workspace_size.argtypes = [I, I, I, I, I]
         lib.pa_mixed_step.restype = I
         lib.pa_mixed_step.argtypes = [PP, P, P, P, I, I, I, P, P, I, F, I, P, P, P, P, SZ, P, P]
+        lib.pa_mixed_step_with_units.restype = I
+        lib.pa_mixed_step_with_units.argtypes = [PP, P, P, P, I, I, I, P, P, I, F, I, P, P, P, I, P,
+                                                 SZ, P, P]
         lib.pa_decode_with_ctas.restype = I
         lib.pa_decode_with_ctas.argtypes = [PP, P, P, I, I, P, I, P, F, I, P, SZ, P, P]
         lib.pa_decode_static_ws.restype = I
@@ -331,6 +334,22 @@ def pa_mixed_step(out, q, cu_q_lens, context_lens, block_tables, k_pool, v_pool,
                   token_budget: int, k_new=None, v_new=None, slot_mapping=None, workspace=None,
                   d_status=None, stream=None):
     """Mixed decode + prefill-chunk step, q/out [T, Hq, d]. Returns out."""
+    return _mixed(None, out, q, cu_q_lens, context_lens, block_tables, k_pool, v_pool, scale,
+                  token_budget, k_new, v_new, slot_mapping, workspace, d_status, stream)
+
+
+def pa_mixed_step_with_units(out, q, cu_q_lens, context_lens, block_tables, k_pool, v_pool,
+                             scale: float, token_budget: int, prefill_q_tiles: int, k_new=None,
+                             v_new=None, slot_mapping=None, workspace=None, d_status=None,
+                             stream=None):
+    """pa_mixed_step with 1 or 2 query tiles per tensor-core prefill unit (0: automatic)."""
+    return _mixed(int(prefill_q_tiles), out, q, cu_q_lens, context_lens, block_tables, k_pool,
+                  v_pool, scale, token_budget, k_new, v_new, slot_mapping, workspace, d_status,
+                  stream)
+
+
+def _mixed(q_tiles, out, q, cu_q_lens, context_lens, block_tables, k_pool, v_pool, scale,
+           token_budget, k_new, v_new, slot_mapping, workspace, d_status, stream):
     lib = load()
     pool = make_pool(k_pool, v_pool)
     T, hq, d = q.shape
@@ -340,10 +359,12 @@ def pa_mixed_step(out, q, cu_q_lens, context_lens, block_tables, k_pool, v_pool,
         raise TypeError("cu_q_lens, block_tables and context_lens must be int32")
     mb = int(block_tables.shape[1])
     ws = _workspace(pa_mixed_workspace_size(S, T, hq, d, mb), q.device, workspace)
-    _check("pa_mixed_step",
-           lib.pa_mixed_step(ctypes.byref(pool), _ptr(out), _ptr(q), _ptr(cu_q_lens), S, T, hq,
-                             _ptr(context_lens), _ptr(block_tables), mb, float(scale),
-                             int(token_budget), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
-                             _ptr(ws), ws.numel() * ws.element_size(), _ptr(d_status),
-                             _stream(stream)))
+    common = (ctypes.byref(pool), _ptr(out), _ptr(q), _ptr(cu_q_lens), S, T, hq,
+              _ptr(context_lens), _ptr(block_tables), mb, float(scale), int(token_budget),
+              _ptr(k_new), _ptr(v_new), _ptr(slot_mapping))
+    tail = (_ptr(ws), ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream))
+    if q_tiles is None:
+        _check("pa_mixed_step", lib.pa_mixed_step(*common, *tail))
+    else:
+        _check("pa_mixed_step_with_units", lib.pa_mixed_step_with_units(*common, q_tiles, *tail))
     return out

@@ -304,6 +304,7 @@ int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q
   pf.pre_ml = pre_ml;
   pf.pre_acc = pre_acc;
   pf.beside_previous = 1;
+  pf.sm_budget = std::max(1, device_sm_count() - a.grid_override);
   // the suffix decode first (it takes its SMs), the prefix pass beside it,
   // then the merge, which folds the prefix partials in, after both
   a.launch_part = 1;
@@ -334,16 +335,18 @@ size_t pa_mixed_workspace_size(int num_seqs, int num_tokens, int num_q_heads, in
   return decode_workspace_bytes(num_seqs, num_q_heads, head_dim);
 }
 
-int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_t* cu_q_lens,
-                  int num_seqs, int num_tokens, int num_q_heads, const int32_t* context_lens,
-                  const int32_t* block_tables, int max_blocks_per_seq, float scale,
-                  int token_budget, const void* k_new, const void* v_new,
-                  const int64_t* slot_mapping, void* workspace, size_t workspace_bytes,
-                  int* d_status, void* stream) {
+int pa_mixed_step_with_units(const pa_kv_pool* pool, void* out, const void* q,
+                             const int32_t* cu_q_lens, int num_seqs, int num_tokens,
+                             int num_q_heads, const int32_t* context_lens,
+                             const int32_t* block_tables, int max_blocks_per_seq, float scale,
+                             int token_budget, const void* k_new, const void* v_new,
+                             const int64_t* slot_mapping, int prefill_q_tiles, void* workspace,
+                             size_t workspace_bytes, int* d_status, void* stream) {
   pa::TraceRange trace("pa_mixed_step");
   int rc = check_pool(pool);
   if (rc != PA_OK) return rc;
   if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq <= 0) return PA_EINVAL;
+  if (prefill_q_tiles < 0 || prefill_q_tiles > 2) return PA_EINVAL;
   rc = check_heads(pool, num_q_heads);
   if (rc != PA_OK) return rc;
   if (num_tokens > token_budget) return PA_EBUDGET;
@@ -389,6 +392,7 @@ int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_
   pf.context_lens = context_lens;
   pf.scale = scale;
   pf.d_status = d_status;
+  pf.q_tiles = prefill_q_tiles;
   DecodeArgs a = {};
   a.pool = view(pool);
   a.out = out;
@@ -416,6 +420,7 @@ int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_
     rc = to_status(launch_decode(a, st));
     if (rc != PA_OK) return rc;
     pf.beside_previous = 1;
+    pf.sm_budget = std::max(1, device_sm_count() - a.grid_override);
     rc = to_status(launch_prefill(pf, st));
     if (rc != PA_OK) return rc;
     a.launch_part = 2;
@@ -424,6 +429,18 @@ int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_
   rc = to_status(launch_prefill(pf, st));
   if (rc != PA_OK) return rc;
   return to_status(launch_decode(a, st));
+}
+
+int pa_mixed_step(const pa_kv_pool* pool, void* out, const void* q, const int32_t* cu_q_lens,
+                  int num_seqs, int num_tokens, int num_q_heads, const int32_t* context_lens,
+                  const int32_t* block_tables, int max_blocks_per_seq, float scale,
+                  int token_budget, const void* k_new, const void* v_new,
+                  const int64_t* slot_mapping, void* workspace, size_t workspace_bytes,
+                  int* d_status, void* stream) {
+  return pa_mixed_step_with_units(pool, out, q, cu_q_lens, num_seqs, num_tokens, num_q_heads,
+                                  context_lens, block_tables, max_blocks_per_seq, scale,
+                                  token_budget, k_new, v_new, slot_mapping, 0, workspace,
+                                  workspace_bytes, d_status, stream);
 }
 
 }  // extern "C"

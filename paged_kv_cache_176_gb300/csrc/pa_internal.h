@@ -101,6 +101,11 @@ struct PrefillArgs {
   // kernel on the SMs it leaves free; the prefill reads nothing that kernel
   // writes and never waits for it
   int beside_previous;
+  // SMs the prefill can expect to run on (0: all of them); with fewer, it
+  // favours more, smaller units
+  int sm_budget;
+  // Q tiles of 128 rows per tensor-core unit (1 or 2); 0: chosen from the sizes
+  int q_tiles;
 };
 bool prefill_supported(int dtype, int head_dim, int group);
 // the tensor-core kernel in prefix mode (bf16, head_dim 128)

@@ -9,30 +9,36 @@
 // through the sequence's block table (K_r = gather(K_pool, table_r), the
 // gather figure of the "C13 L2 serving" page).
 //
-// GB300 design (one CTA per 128 query rows of one KV head):
-//  * The 128 rows are 128/G tokens x the G query heads that share the KV head,
-//    so one K/V tile in shared memory serves the whole GQA group.
-//  * Warp 0 moves Q once and then K tiles of 128 keys (8 pool blocks) into a
-//    three-stage ring, warp 10 moves V tiles into a two-stage ring; each block
-//    is one 3-D tiled TMA copy (64 head-dim columns x 16 tokens, 128-byte
-//    swizzle) straight out of the paged pool, so the gather costs no extra pass.
-//  * Warp 1 owns 512 TMEM columns and issues the MMAs from one thread:
-//    S = Q K^T (128 x 128, fp32, double-buffered in TMEM) and, per key half,
-//    O_h += P_h V_h with P_h read from TMEM (the A operand of a TS-MMA) and
-//    V_h (64 keys x head_dim) from shared memory; tcgen05.commit signals
-//    the mbarriers.
-//  * Warps 2-9 hold two threads per query row, one per half of the key tile.
-//    Each reads its 64 S columns from TMEM, applies the causal mask and the
-//    online softmax in the log2 domain with its own (max, sum), writes P as
-//    bf16 pairs back into the S columns it read, and rescales its own O_h only
-//    when its max grows by more than 8 (lazy rescaling). Masked keys get
-//    weight 0. The epilogue merges the two halves' (max, sum, O_h).
-//  * On the last key tile each half zeroes the value rows of its own 64 keys
-//    that lie past the context or past the loaded blocks, before it hands P_h
-//    to the MMA that reads exactly those rows, so stale or NaN slots never
-//    reach the result.
-//  * Every wait is bounded; a timeout sets PA_STATUS_TIMEOUT and the CTA
-//    leaves after releasing its TMEM.
+// GB300 design: one CTA per unit of one KV head, a unit being one or two Q
+// tiles of 128 rows (128/G consecutive tokens x the G query heads that share
+// the KV head), so that one K/V tile in shared memory serves up to 256 rows.
+//  * Warp 0 moves the Q tiles once and then K tiles of 128 keys (8 pool
+//    blocks) into a two-stage ring, warp 10 moves V tiles into a two-stage
+//    ring; each block is one 3-D tiled TMA copy (64 head-dim columns x 16
+//    tokens, 128-byte swizzle) straight out of the paged pool, so the gather
+//    costs no extra pass.
+//  * Warp 1 owns all 512 TMEM columns (S and O of each Q tile, 128 columns
+//    each) and issues the MMAs from one thread: S_x = Q_x K^T (128 x 128,
+//    fp32) and O_x += P_x V with P_x read from TMEM (the A operand of a
+//    TS-MMA) and V (128 keys x head_dim) from shared memory. The two Q tiles
+//    alternate: while the softmax of one tile runs, the tensor pipe works on
+//    the other's products, and S_x(j+1) follows P_x(j) V(j) in the pipe.
+//  * Warps 2-5 (Q tile 0) and 6-9 (Q tile 1) hold one thread per query row.
+//    Each reads its row of S from TMEM and writes P = 2^(s - m) as bf16 pairs
+//    over the first 64 columns it read, m being its running max in the log2
+//    domain. The max moves only when a score exceeds it by more than 8 (lazy
+//    rescaling), and the row sum bounds every weight: while the sum stays at
+//    or below 2^8 no score passed m + 8, so the tile needs no max pass. Only
+//    otherwise (and on the first tile) is the row's max taken and P redone
+//    with it, O rescaled in TMEM when the max moved. Masked keys get weight 0.
+//  * On the last key tile the rows of Q tile 0 zero the value rows that lie
+//    past the context or past the loaded blocks, before P_0 goes to the MMA,
+//    so stale or NaN slots never reach the result.
+//  * Units run longest first: every CTA finds the unit of its rank in the
+//    order of decreasing key-tile count from the chunk lengths alone.
+//  * Every wait is bounded; a timeout sets PA_STATUS_TIMEOUT, the roles stop,
+//    wait (bounded) for their copies and MMAs in flight, and the CTA releases
+//    its TMEM and leaves.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,29 +51,28 @@ namespace pa {
 namespace {
 
 constexpr int kD = 128;              // head_dim of the tensor-core path
-constexpr int kRowsTile = 128;       // query rows per CTA (MMA M)
+constexpr int kRowsTile = 128;       // query rows per Q tile (MMA M)
 constexpr int kKeysTile = 128;       // keys per tile (MMA N of Q K^T)
 constexpr int kBlocksTile = kKeysTile / kBlockSize;
-constexpr int kThreadsTc = 352;      // warp 0 K loads, warp 1 MMA, warps 2-9 softmax, warp 10 V loads
+constexpr int kThreadsTc = 352;      // warp 0 Q/K loads, warp 1 MMA, warps 2-9 softmax, warp 10 V loads
 constexpr int kVWarp = 10;
 constexpr int kHalf = 16384;         // one 64-column half of a 128-row bf16 tile
 constexpr int kTileBytes = 2 * kHalf;
-constexpr int kKStages = 3;          // K is released as soon as S = Q K^T is done
-constexpr int kVStages = 2;          // V is released after O += P V
+constexpr int kKStages = 2;          // K is released as soon as both S = Q K^T are done
+constexpr int kVStages = 2;          // V is released after both O += P V
 
 // shared memory layout (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kOffQ = 0;                               // Q tiles 0 and 1
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffP = kOffV + kVStages * kTileBytes;  // also holds the tile prefix at start-up
-constexpr int kOffBar = kOffP + kTileBytes;
-constexpr int kSmemTc = kOffBar + 256 + 1024;         // + barriers + alignment slack
-constexpr int kMaxPrefixSeqs = kTileBytes / 4 - 1;
+constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+constexpr int kSmemTc = kOffBar + 256 + 1024;          // + barriers + alignment slack
+constexpr int kMaxPrefixSeqs = 8191;                   // sequences (groups) per launch
 
-// TMEM columns
+// TMEM columns: S of Q tile x at 128 x, O of Q tile x at 256 + 128 x
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0;     // S buffers at 0 and 128
-constexpr uint32_t kColO = 256;    // O accumulators: keys 0-63 of every tile at 256, keys 64-127 at 384
+__device__ __forceinline__ uint32_t col_s(int x) { return static_cast<uint32_t>(x) * 128u; }
+__device__ __forceinline__ uint32_t col_o(int x) { return 256u + static_cast<uint32_t>(x) * 128u; }
 
 struct TcParams {
   const int32_t* cu_q_lens;
@@ -75,6 +80,7 @@ struct TcParams {
   const int32_t* block_tables;
   void* out;
   int num_seqs, num_rows, hq, hkv, group, max_blocks;
+  int q_tiles;  // Q tiles per unit: 1 or 2
   int64_t num_blocks;
   float scale_log2;
   int* d_status;
@@ -89,29 +95,107 @@ struct TcBarriers {
   uint64_t k_empty[kKStages];
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
-  uint64_t s_full[2];
-  uint64_t s_empty[2];
-  uint64_t p_full[2][2];  // [S buffer][key half]: P of one 64-key half written
-  uint64_t pv_done;
+  uint64_t s_full[2];   // [Q tile]: S = Q K^T of the current key tile is in TMEM
+  uint64_t p_full[2];   // [Q tile]: its P is in TMEM (one arrival per softmax warp)
+  uint64_t pv_done[2];  // [Q tile]: O += P V of the current key tile is complete
+  uint64_t drain;       // the issuer's last MMAs are complete
   uint32_t tmem_base;
   int bad_block;
   int abort;
 };
 static_assert(sizeof(TcBarriers) <= 256, "barrier block");
 
-__device__ __forceinline__ int tc_tiles(const TcParams& p, int s, int tq) {
+// ---------------------------------------------------------------- unit order
+
+// Units of sequence s (rows of up to T tokens): prefill chunks of two or more
+// rows (single rows are decode rows); in prefix mode any non-empty group with
+// a non-empty shared prefix.
+__device__ __forceinline__ int units_of(const TcParams& p, int s, int T, int* q_len, int* ctx) {
   const int q0 = p.cu_q_lens[s], q1 = p.cu_q_lens[s + 1];
-  // prefill: chunks of two or more rows (single rows are decode rows);
-  // prefix mode: any non-empty group with a non-empty shared prefix
+  *q_len = q1 - q0;
+  *ctx = p.context_lens[s];
   if (q0 < 0 || q1 > p.num_rows || q1 - q0 < (p.prefix_mode ? 1 : 2)) return 0;
-  if (p.prefix_mode && p.context_lens[s] <= 0) return 0;
-  return (q1 - q0 + tq - 1) / tq;
+  if (p.prefix_mode && *ctx <= 0) return 0;
+  return (q1 - q0 + T - 1) / T;
+}
+
+// Units of sequence s that read at least V key tiles (every unit for V <= 1).
+// Unit u's rows end at token f(u) = min((u + 1) T, q_len) - 1, position
+// ctx - q_len + f(u), so it reads (ctx - q_len + f(u)) / 128 + 1 key tiles;
+// f grows with u, so these units are the last ones of the sequence.
+__device__ __forceinline__ int units_at_least(const TcParams& p, int s, int T, int V) {
+  int q_len, ctx;
+  const int U = units_of(p, s, T, &q_len, &ctx);
+  if (U == 0 || V <= 1) return U;
+  if (p.prefix_mode) return (ctx - 1) / kKeysTile + 1 >= V ? U : 0;
+  // need min((u + 1) T, q_len) >= R
+  const int64_t R = static_cast<int64_t>(kKeysTile) * (V - 1) + 1 - (static_cast<int64_t>(ctx) - q_len);
+  if (R > q_len) return 0;
+  const int64_t u_first = R <= T ? 0 : (R + T - 1) / T - 1;
+  return U - static_cast<int>(u_first);
+}
+
+// Units of all sequences reading at least V key tiles, summed by one warp.
+__device__ __forceinline__ int warp_count_at_least(const TcParams& p, int T, int V, int lane) {
+  int c = 0;
+  for (int s = lane; s < p.num_seqs; s += 32) c += units_at_least(p, s, T, V);
+  return __reduce_add_sync(0xffffffffu, c);
+}
+
+// The unit of rank k (0-based) in the order of decreasing key-tile count
+// (ties by sequence, then unit): its sequence and unit index, or false when
+// there are at most k units. Computed by each warp on its own.
+__device__ __forceinline__ bool unit_of_rank(const TcParams& p, int T, int k, int lane, int* s_out,
+                                             int* u_out) {
+  const int v_top = (p.max_blocks * kBlockSize - 1) / kKeysTile + 1;
+  if (warp_count_at_least(p, T, 1, lane) <= k) return false;
+  // largest V in [1, v_top] with more than k units reading at least V tiles
+  int lo = 1, hi = v_top;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (warp_count_at_least(p, T, mid, lane) > k) lo = mid; else hi = mid - 1;
+  }
+  const int v = lo;
+  const int above = v == v_top ? 0 : warp_count_at_least(p, T, v + 1, lane);
+  int r = k - above;  // rank among the units whose count is v (>= v_top at the top)
+  for (int base = 0; base < p.num_seqs; base += 32) {
+    const int s = base + lane;
+    int first = 0, e = 0;
+    if (s < p.num_seqs) {
+      int q_len, ctx;
+      const int U = units_of(p, s, T, &q_len, &ctx);
+      const int at = units_at_least(p, s, T, v);
+      const int over = v == v_top ? 0 : units_at_least(p, s, T, v + 1);
+      first = U - at;
+      e = at - over;
+    }
+    int incl = e;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, e > 0 && incl - e <= r && r < incl);
+    if (hit != 0) {
+      const int src = __ffs(hit) - 1;
+      *s_out = base + src;
+      *u_out = __shfl_sync(0xffffffffu, first + (r - (incl - e)), src);
+      return true;
+    }
+    r -= __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return false;  // not reached: the counts cover every unit
 }
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h2);
 }
 
 }  // namespace
@@ -127,28 +211,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   extern __shared__ char smem_raw[];
   char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   TcBarriers& bar = *reinterpret_cast<TcBarriers*>(smem + kOffBar);
-  __shared__ int warp_sums[kThreadsTc / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.group;
-  const int tq = kRowsTile / G;  // tokens per tile
-  const int g = blockIdx.y;      // KV head
-
-  // this CTA's (sequence, tile); tiles run from the last (longest) one down.
-  // The prefix lives in the P buffer, which is free until the softmax starts.
-  int* prefix = reinterpret_cast<int*>(smem + kOffP);
-  block_exclusive_scan<kThreadsTc>(
-      p.num_seqs, [&](int i) { return tc_tiles(p, i, tq); }, prefix, warp_sums);
-  const int total = prefix[p.num_seqs];
-  if (static_cast<int>(blockIdx.x) >= total) return;
-  const int t_global = total - 1 - static_cast<int>(blockIdx.x);
-  const int s = upper_index(prefix, p.num_seqs, t_global);
-  const int tile = t_global - prefix[s];
+  const int tq = kRowsTile / G;  // tokens per Q tile
+  const int T = tq * p.q_tiles;  // tokens per unit
+  // CTA rank k: unit rank k / hkv, KV head k % hkv, longest units first
+  const int k_rank = static_cast<int>(blockIdx.x);
+  const int g = k_rank % p.hkv;
+  int s = 0, unit = 0;
+  if (!unit_of_rank(p, T, k_rank / p.hkv, lane, &s, &unit)) return;
   const int q0 = p.cu_q_lens[s];
   const int q_len = p.cu_q_lens[s + 1] - q0;
   const int ctx = p.context_lens[s];
-  const int tok0 = tile * tq;
-  const int ntok = min(tq, q_len - tok0);
+  const int tok0 = unit * T;
+  const int ntok = min(T, q_len - tok0);          // tokens of this unit
+  const int nq = (ntok + tq - 1) / tq;             // Q tiles with rows: 1 or 2
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   const bool bad_len = p.prefix_mode ? (ctx % kBlockSize != 0 || ctx > p.max_blocks * kBlockSize)
                                      : (q_len > ctx || ctx > p.max_blocks * kBlockSize);
@@ -166,7 +244,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     return;
   }
-  // Absolute position of the tile's first row; in prefix mode every row sits
+  // Absolute position of the unit's first row; in prefix mode every row sits
   // past the whole prefix (a decode token after it) and sees all its keys.
   const int pos0 = p.prefix_mode ? ctx - 1 : ctx - q_len + tok0;
   const int max_pos = p.prefix_mode ? pos0 : pos0 + ntok - 1;  // last row's absolute position
@@ -183,13 +261,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mbar_init(&bar.v_full[i], 1);
       mbar_init(&bar.v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar.s_full[i], 1);
-      mbar_init(&bar.s_empty[i], 8);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar.s_full[x], 1);
+      mbar_init(&bar.p_full[x], 4);
+      mbar_init(&bar.pv_done[x], 1);
     }
-    for (int b = 0; b < 2; ++b)
-      for (int h = 0; h < 2; ++h) mbar_init(&bar.p_full[b][h], 4);
-    mbar_init(&bar.pv_done, 1);
+    mbar_init(&bar.drain, 1);
     bar.bad_block = 0;
     bar.abort = 0;
     fence_mbar_init();
@@ -202,6 +279,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = bar.tmem_base;
+  auto fail = [&]() {
+    atomicOr(&bar.abort, 1);
+    status_or(p.d_status, PA_STATUS_TIMEOUT);
+  };
 
   // Block-table entries of key tile j, read as one batch of independent loads.
   auto tile_blocks = [&](int j, int (&ph)[kBlocksTile]) -> int {
@@ -215,16 +296,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     return nb;
   };
   // One producer per operand: TMA of K tiles (warp 0) or V tiles (warp 10),
-  // each 128 keys = 8 pool blocks x two 64-column halves.
+  // each 128 keys = 8 pool blocks x two 64-column halves. On leaving, it waits
+  // (bounded) for the copies of the stages it filled last.
   auto produce = [&](const CUtensorMap* tm, int off, int stages, uint64_t* full, uint64_t* empty) {
     int ph[kBlocksTile], phn[kBlocksTile];
     int nb = tile_blocks(0, ph);
+    int issued = 0;
     for (int j = 0; j < n_kt; ++j) {
       const int st = j % stages;
       const int nbn = j + 1 < n_kt ? tile_blocks(j + 1, phn) : 0;  // prefetch the next tile's table
-      if (!mbar_wait_bounded(&empty[st], ((j / stages) & 1) ^ 1)) {
-        atomicOr(&bar.abort, 1);
-        return;
+      if (bar.abort != 0 || !mbar_wait_bounded(&empty[st], ((j / stages) & 1) ^ 1)) {
+        if (bar.abort == 0) fail();
+        break;
       }
       char* dst = smem + off + st * kTileBytes;
       mbar_arrive_expect_tx(&full[st], nb * 2 * (kBlockSize * 128));
@@ -239,10 +322,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc::tma_load_3d(dst + b * (kBlockSize * 128), tm, 0, g, row, &full[st]);
         tc::tma_load_3d(dst + kHalf + b * (kBlockSize * 128), tm, 64, g, row, &full[st]);
       }
+      issued = j + 1;
 #pragma unroll
       for (int b = 0; b < kBlocksTile; ++b) ph[b] = phn[b];
       nb = nbn;
     }
+    for (int j = max(0, issued - stages); j < issued; ++j)
+      mbar_wait_bounded(&full[j % stages], (j / stages) & 1);
   };
 
   if (warp == 0) {
@@ -250,10 +336,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_k);
-      mbar_arrive_expect_tx(&bar.q_full, 2 * kHalf);
-      tc::tma_load_3d(smem + kOffQ, &tm_q, 0, g * G, q0 + tok0, &bar.q_full);
-      tc::tma_load_3d(smem + kOffQ + kHalf, &tm_q, 64, g * G, q0 + tok0, &bar.q_full);
+      mbar_arrive_expect_tx(&bar.q_full, nq * 2 * kHalf);
+      for (int x = 0; x < nq; ++x) {
+        char* dq = smem + kOffQ + x * kTileBytes;
+        tc::tma_load_3d(dq, &tm_q, 0, g * G, q0 + tok0 + x * tq, &bar.q_full);
+        tc::tma_load_3d(dq + kHalf, &tm_q, 64, g * G, q0 + tok0 + x * tq, &bar.q_full);
+      }
       produce(&tm_k, kOffK, kKStages, bar.k_full, bar.k_empty);
+      mbar_wait_bounded(&bar.q_full, 0);
     }
   } else if (warp == kVWarp) {
     // ------------------------------------------------------------ V loads
@@ -266,270 +356,257 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (lane == 0) {
       const uint32_t id_qk = tc::idesc_bf16_f32(kRowsTile, kKeysTile, false, false);
       const uint32_t id_pv = tc::idesc_bf16_f32(kRowsTile, kD, false, true);
-      const uint32_t sQ = smem_addr(smem + kOffQ);
-      const uint32_t sP = smem_addr(smem + kOffP);
-      // S(j) = Q K_j^T into TMEM buffer j % 2; K_j's stage is free when it completes
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kKStages;
-        if (!mbar_wait_bounded(&bar.k_full[st], (j / kKStages) & 1)) return false;
+      auto wait = [&](uint64_t* b, uint32_t parity) -> bool {
+        if (bar.abort != 0 || !mbar_wait_bounded(b, parity)) return false;
         tc::fence_after_sync();
-        const uint32_t sK = smem_addr(smem + kOffK + st * kTileBytes);
+        return true;
+      };
+      // S_x = Q_x K_j^T into S_x's columns (K_j's stage is full)
+      auto issue_s = [&](int x, int j) {
+        const uint32_t sQ = smem_addr(smem + kOffQ + x * kTileBytes);
+        const uint32_t sK = smem_addr(smem + kOffK + (j % kKStages) * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + kColS0 + (j & 1) * kKeysTile, tc::smem_desc(sQ + o, 16, 1024),
+          tc::mma_bf16(tmem + col_s(x), tc::smem_desc(sQ + o, 16, 1024),
                        tc::smem_desc(sK + o, 16, 1024), id_qk, kk > 0);
         }
-        tc::mma_commit(&bar.s_full[j & 1]);
-        tc::mma_commit(&bar.k_empty[st]);
-        return true;
+        tc::mma_commit(&bar.s_full[x]);
       };
-      bool ok = mbar_wait_bounded(&bar.q_full, 0);
-      if (ok) ok = issue_s(0);
-      if (ok && n_kt > 1) ok = issue_s(1);
-      for (int j = 0; ok && j < n_kt; ++j) {
-        const int vs = j % kVStages;
-        if (!mbar_wait_bounded(&bar.v_full[vs], (j / kVStages) & 1)) {
-          ok = false;
-          break;
-        }
-        const uint32_t sV = smem_addr(smem + kOffV + vs * kTileBytes);
-        // O_h += P_h V_h for the two 64-key halves, each as soon as its P is
-        // in TMEM (P_h sits in the first 32 columns of S_j's h-th half)
-        for (int h = 0; h < 2 && ok; ++h) {
-          // one barrier pair per S buffer: the next arrival on it needs
-          // S(j + 2), which is issued only after this wait
-          if (!mbar_wait_bounded(&bar.p_full[j & 1][h], (j >> 1) & 1)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint32_t pcol = tmem + kColS0 + (j & 1) * kKeysTile + h * (kKeysTile / 2);
+      // O_x += P_x V_j: key group kk (16 keys) is P columns 8 kk .. 8 kk + 7
+      auto issue_pv = [&](int x, int j) {
+        const uint32_t sV = smem_addr(smem + kOffV + (j % kVStages) * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16_ts(tmem + kColO + h * kD, pcol + kk * 8,
-                            tc::smem_desc(sV + (4 * h + kk) * (16 * 128), kHalf, 1024), id_pv,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kKeysTile / 16; ++kk)
+          tc::mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8,
+                          tc::smem_desc(sV + kk * (16 * 128), kHalf, 1024), id_pv,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(&bar.pv_done[x]);
+      };
+      const bool two = nq == 2;
+      bool ok = wait(&bar.q_full, 0) && wait(&bar.k_full[0], 0);
+      if (ok) {
+        issue_s(0, 0);
+        if (two) issue_s(1, 0);
+        tc::mma_commit(&bar.k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_kt; ++j) {
+        const bool next = j + 1 < n_kt;
+        const int ks = (j + 1) % kKStages;
+        ok = wait(&bar.v_full[j % kVStages], (j / kVStages) & 1) && wait(&bar.p_full[0], j & 1);
         if (!ok) break;
-        tc::mma_commit(&bar.v_empty[vs]);
-        tc::mma_commit(&bar.pv_done);
-        // S(j + 2) reuses S_j's columns: the tensor pipe runs it after P_j V_j
-        if (j + 2 < n_kt && !issue_s(j + 2)) {
-          ok = false;
-          break;
+        issue_pv(0, j);
+        // S_0(j+1) overwrites P_0(j), which the pipe reads first
+        if (next) {
+          if (!(ok = wait(&bar.k_full[ks], ((j + 1) / kKStages) & 1))) break;
+          issue_s(0, j + 1);
+        }
+        if (two) {
+          if (!(ok = wait(&bar.p_full[1], j & 1))) break;
+          issue_pv(1, j);
+        }
+        tc::mma_commit(&bar.v_empty[j % kVStages]);
+        if (next) {
+          if (two) issue_s(1, j + 1);
+          tc::mma_commit(&bar.k_empty[ks]);
         }
       }
-      if (!ok) atomicOr(&bar.abort, 1);
+      if (!ok && bar.abort == 0) fail();
+      tc::mma_commit(&bar.drain);
+      mbar_wait_bounded(&bar.drain, 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Two threads per query row: half hf owns keys 64*hf .. 64*hf+63 of every
-    // tile and runs its own online softmax into its own O accumulator; the
-    // two (max, sum, O) triples are merged once, in the epilogue.
+    // One thread per query row: warps 2-5 own Q tile 0, warps 6-9 Q tile 1.
+    const int x = (warp - 2) >> 2;             // Q tile
     const int quad = warp & 3;                 // TMEM lane quarter this warp may access
-    const int hf = (warp - 2) >> 2;            // key half
-    const int r = quad * 32 + lane;            // tile row owned by this thread
-    const int ri = r / G;                      // token of the row within the tile
-    const int pos = ri < ntok ? pos0 + (p.prefix_mode ? 0 : ri) : -1;  // absolute position (-1: padding row)
+    const int r = quad * 32 + lane;            // row within the Q tile
+    const int ti = x * tq + r / G;             // token of the row within the unit
+    const bool live = ti < ntok;
+    const int pos = live ? pos0 + (p.prefix_mode ? 0 : x * tq + r / G) : -1;  // absolute position
+    const int pos_first = p.prefix_mode ? pos0 : pos0 + x * tq;              // the tile's first row
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const uint32_t ocol = kColO + hf * kD;     // this half's O accumulator
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    constexpr int kCols = kKeysTile / 2;
-    for (int j = 0; j < n_kt; ++j) {
-      const int buf = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.s_full[buf], (j >> 1) & 1));
-      if (!ok) break;
-      tc::fence_after_sync();
-      float sc[kCols];
-      {
-        uint32_t raw[2][32];
+    const uint32_t scol = trow + col_s(x), ocol = trow + col_o(x);
+    const float sl2 = p.scale_log2;
+    // rows past the unit keep m = +inf: every weight is 0 and nothing moves
+    float m = live ? -INFINITY : INFINITY, l = 0.f;
+    bool ok = x < nq;
+    // P = 2^(s - mm) of this row's 128 keys (0 past the row's position) into
+    // pk; returns the row sum
+    auto weights = [&](float mm, bool full, int key0, uint32_t (&pk)[64]) -> float {
+      float2 acc[4];
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          tc::tmem_ld32(trow + kColS0 + buf * kKeysTile + hf * kCols + c * 32, raw[c]);
-        tc::tmem_wait_ld();
+      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+      if (full) {
+        const float2 c2 = make_float2(sl2, sl2);
+        const float2 nm = make_float2(-mm, -mm);
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int h = 0; h < 2; ++h) {
+          uint32_t raw[2][32];
+          tc::tmem_ld32(scol + h * 64, raw[0]);
+          tc::tmem_ld32(scol + h * 64 + 32, raw[1]);
+          tc::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) sc[c * 32 + e] = __uint_as_float(raw[c][e]);
-      }
-      // Key halves entirely below the diagonal need no mask (every key <=
-      // every row's position); the others mask keys past each row's position.
-      const int key0 = j * kKeysTile + hf * kCols;
-      const bool full = key0 + kCols - 1 <= pos0 && p.scale_log2 > 0.f;
-      float mx;
-      {
-        float mp[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < kCols; ++c) mp[c & 7] = fmaxf(mp[c & 7], sc[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < kCols; ++c) {
-            const float v = (key0 + c <= pos) ? sc[c] * p.scale_log2 : -INFINITY;
-            sc[c] = v;
-            mp[c & 7] = fmaxf(mp[c & 7], v);
+          for (int c = 0; c < 32; ++c) {
+            const float2 sv = make_float2(__uint_as_float(raw[c >> 4][(2 * c) & 31]),
+                                          __uint_as_float(raw[c >> 4][(2 * c + 1) & 31]));
+            const float2 t = __ffma2_rn(sv, c2, nm);
+            const float2 w = make_float2(ex2(t.x), ex2(t.y));
+            acc[c & 3] = __fadd2_rn(acc[c & 3], w);
+            pk[h * 32 + c] = pack_bf16(w.x, w.y);
           }
         }
-        mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-        if (full) mx *= p.scale_log2;  // scores in the log2 domain
-      }
-      // lazy running max: move it only when a score exceeds it by more than 8
-      const bool need = mx > m + 8.f;
-      const bool warp_need = __any_sync(0xffffffffu, need);
-      const float mn = need ? mx : m;
-      const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2(m - mn) : 1.f);
-      m = mn;
-      // P = 2^(s - m) in registers (bf16 pairs) before touching shared P
-      uint32_t pk[kCols / 2];
-      float2 rsp[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) rsp[i] = make_float2(0.f, 0.f);
-      if (full) {
-        const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-        const float2 nm = make_float2(-m, -m);
-#pragma unroll
-        for (int c = 0; c < kCols / 2; ++c) {
-          const float2 t = __ffma2_rn(make_float2(sc[2 * c], sc[2 * c + 1]), c2, nm);
-          const float2 w = make_float2(ex2(t.x), ex2(t.y));
-          rsp[c & 3] = __fadd2_rn(rsp[c & 3], w);
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(w.x, w.y);
-          pk[c] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
       } else {
+        // tiles that cross a row's position: keys past it get weight 0
 #pragma unroll
-        for (int c = 0; c < kCols / 2; ++c) {
-          const float a = sc[2 * c], b = sc[2 * c + 1];
-          const float2 w = make_float2(a == -INFINITY ? 0.f : ex2(a - m), b == -INFINITY ? 0.f : ex2(b - m));
-          rsp[c & 3] = __fadd2_rn(rsp[c & 3], w);
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(w.x, w.y);
-          pk[c] = *reinterpret_cast<const uint32_t*>(&h2);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t raw[2][32];
+          tc::tmem_ld32(scol + h * 64, raw[0]);
+          tc::tmem_ld32(scol + h * 64 + 32, raw[1]);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int key = key0 + h * 64 + 2 * c;
+            const float a = key <= pos ? __uint_as_float(raw[c >> 4][(2 * c) & 31]) * sl2 : -INFINITY;
+            const float b = key + 1 <= pos ? __uint_as_float(raw[c >> 4][(2 * c + 1) & 31]) * sl2 : -INFINITY;
+            const float2 w = make_float2(a == -INFINITY ? 0.f : ex2(a - mm), b == -INFINITY ? 0.f : ex2(b - mm));
+            acc[c & 3] = __fadd2_rn(acc[c & 3], w);
+            pk[h * 32 + c] = pack_bf16(w.x, w.y);
+          }
         }
       }
-      const float rs = ((rsp[0].x + rsp[0].y) + (rsp[1].x + rsp[1].y)) +
-                       ((rsp[2].x + rsp[2].y) + (rsp[3].x + rsp[3].y));
+      return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+    };
+    // the row's largest score of the tile in the log2 domain (-inf if none)
+    auto row_max = [&](int key0) -> float {
+      float mp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t raw[2][32];
+        tc::tmem_ld32(scol + h * 64, raw[0]);
+        tc::tmem_ld32(scol + h * 64 + 32, raw[1]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const float v = key0 + h * 64 + e <= pos ? __uint_as_float(raw[e >> 5][e & 31]) * sl2 : -INFINITY;
+          mp[e & 7] = fmaxf(mp[e & 7], v);
+        }
+      }
+      return fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+    };
+    for (int j = 0; ok && j < n_kt; ++j) {
+      ok = __all_sync(0xffffffffu, bar.abort == 0 && mbar_wait_bounded(&bar.s_full[x], j & 1));
+      if (!ok) break;
+      tc::fence_after_sync();
+      const int key0 = j * kKeysTile;
+      // every row of the tile sees every key of this tile: no mask
+      const bool full = key0 + kKeysTile - 1 <= pos_first && sl2 > 0.f;
+      uint32_t pk[64];
+      float rs, alpha = 1.f;
+      bool warp_moved = false;
+      // P with the running max; a weight above 2^8 is possible only if the
+      // sum is, and then the row's max is taken and P redone if it moved
+#pragma unroll 1
+      for (int pass = 0;; ++pass) {
+        rs = weights(m, full, key0, pk);
+        if (pass > 0 || !__any_sync(0xffffffffu, !(rs <= 256.f))) break;
+        const float mx = row_max(key0);
+        const bool need = mx > m + 8.f;
+        warp_moved = __any_sync(0xffffffffu, need);
+        if (!warp_moved) break;
+        const float mn = need ? mx : m;
+        alpha = (m == -INFINITY) ? 0.f : (need ? ex2(m - mn) : 1.f);
+        m = mn;
+      }
       l = l * alpha + rs;
-      // O_hf holds tiles 0 .. j-1 once P_{j-1} V_{j-1} is complete: rescale
-      // this warp's rows only when its running max moved
-      if (j > 0 && warp_need) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.pv_done, (j - 1) & 1));
+      // O holds key tiles 0 .. j-1 once P(j-1) V(j-1) is complete: rescale
+      // this warp's rows only when a max moved
+      if (j > 0 && warp_moved) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.pv_done[x], (j - 1) & 1));
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll
         for (int c = 0; c < kD / 32; ++c) {
           uint32_t o[32];
-          tc::tmem_ld32(trow + ocol + c * 32, o);
+          tc::tmem_ld32(ocol + c * 32, o);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tc::tmem_st32(trow + ocol + c * 32, o);
+          tc::tmem_st32(ocol + c * 32, o);
         }
       }
-      // P (bf16 pairs) over the first 32 columns of this half's S columns
-      tc::tmem_st32(trow + kColS0 + buf * kKeysTile + hf * kCols, pk);
+      // P (bf16 pairs, keys 2c and 2c + 1 in column c) over the first 64 S columns
+      tc::tmem_st64(scol, pk);
       tc::tmem_wait_st();
-      // last tile: zero the value rows no key of this CTA may use. O_h += P_h V_h
-      // reads keys 64*hf .. 64*hf+63 over all head_dim columns, so the 128
-      // threads of this half clear exactly those rows (thread r: key
-      // 64*hf + r/2, head_dim columns 64*(r&1) .. +63) before they arrive
-      // on p_full[buf][hf].
-      if (j == n_kt - 1) {
+      // last tile: Q tile 0's rows zero the value rows no key of this unit may
+      // use (thread r: key row r, both 64-column halves) before P_0 goes to
+      // the MMA; P_1 V follows P_0 V in the pipe
+      if (x == 0 && j == n_kt - 1) {
         const int vs = j % kVStages;
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.v_full[vs], (j / kVStages) & 1));
         if (!ok) break;
         // rows past the context hold stale or poisoned slots; rows past the
         // last loaded block were never written by this CTA
-        const int kr = hf * (kKeysTile / 2) + (r >> 1);
-        if (j * kKeysTile + kr >= min(ctx, nblk * kBlockSize)) {
-          char* sv = smem + kOffV + vs * kTileBytes + (r & 1) * kHalf;
+        if (j * kKeysTile + r >= min(ctx, nblk * kBlockSize)) {
+          char* sv = smem + kOffV + vs * kTileBytes + r * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(sv + kr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.p_full[buf][hf]);
-    }
-    if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.pv_done, (n_kt - 1) & 1));
-      if (ok) tc::fence_after_sync();
-    }
-    if (!ok) atomicOr(&bar.abort, 1);
-    // this half's (max, sum) for the epilogue merge; the P tile is free now
-    float* ml = reinterpret_cast<float*>(smem + kOffP);
-    ml[(hf * kRowsTile + r) * 2] = m;
-    ml[(hf * kRowsTile + r) * 2 + 1] = l;
-  }
-
-  __syncthreads();  // every role done issuing; the last P.V is complete
-  if (warp >= 2 && warp < kVWarp) {
-    const int quad = warp & 3;
-    const int hf = (warp - 2) >> 2;  // this thread writes head_dim columns 64*hf .. 64*hf+63
-    const int r = quad * 32 + lane;
-    const int ri = r / G, rh = r % G;
-    if (bar.abort == 0) {
-      // epilogue: merge the two key halves, O = (a0 O0 + a1 O1) / (a0 l0 + a1 l1)
-      const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-      uint32_t raw[2][2][32];
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) tc::tmem_ld32(trow + kColO + h * kD + hf * 64 + c * 32, raw[h][c]);
-      tc::tmem_wait_ld();
-      if (ri < ntok) {
-        const float* ml = reinterpret_cast<const float*>(smem + kOffP);
-        const float m0 = ml[r * 2], l0 = ml[r * 2 + 1];
-        const float m1 = ml[(kRowsTile + r) * 2], l1 = ml[(kRowsTile + r) * 2 + 1];
-        const float mm = fmaxf(m0, m1);
-        const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mm);
-        const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mm);
-        if (p.prefix_mode) {
-          // the unnormalised partial (max mm, sum, accumulator) of this row
-          const int64_t idx = static_cast<int64_t>(q0 + tok0 + ri) * p.hq + g * G + rh;
-          float* arow = p.pre_acc + idx * kD + hf * 64;
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              float x[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                x[k] = __uint_as_float(raw[0][c][e + k]) * a0 + __uint_as_float(raw[1][c][e + k]) * a1;
-              *reinterpret_cast<float4*>(arow + c * 32 + e) = make_float4(x[0], x[1], x[2], x[3]);
-            }
-          if (hf == 0) p.pre_ml[idx] = make_float2(mm, bar.bad_block ? -1.f : a0 * l0 + a1 * l1);
-        } else {
-        const float inv = bar.bad_block ? 0.f : 1.f / (a0 * l0 + a1 * l1);
-        const float s0 = a0 * inv, s1 = a1 * inv;
-        __nv_bfloat16* orow =
-            out + (static_cast<int64_t>(q0 + tok0 + ri) * p.hq + g * G + rh) * kD + hf * 64;
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int i0 = e + 2 * k;
-              const float x0 = __uint_as_float(raw[0][c][i0]) * s0 + __uint_as_float(raw[1][c][i0]) * s1;
-              const float x1 = __uint_as_float(raw[0][c][i0 + 1]) * s0 + __uint_as_float(raw[1][c][i0 + 1]) * s1;
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-              w[k] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
-            *reinterpret_cast<uint4*>(orow + c * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(sv + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sv + kHalf + c * 16) = make_uint4(0, 0, 0, 0);
           }
         }
+        fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
       }
-    } else if (r == 0 && hf == 0) {
-      status_or(p.d_status, PA_STATUS_TIMEOUT);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.p_full[x]);
+    }
+    if (ok && x < nq) {
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar.pv_done[x], (n_kt - 1) & 1));
+      if (ok) tc::fence_after_sync();
+    }
+    if (x < nq) {
+      if (!ok) {
+        if (lane == 0 && bar.abort == 0) fail();
+      } else {
+        // epilogue: this row's O from TMEM, 32 columns at a time
+        const int rh = r % G;
+        const int64_t idx = static_cast<int64_t>(q0 + tok0 + ti) * p.hq + g * G + rh;
+        const float inv = (bar.bad_block || l == 0.f) ? 0.f : 1.f / l;
+#pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(ocol + c * 32, o);
+          tc::tmem_wait_ld();
+          if (!live) continue;
+          if (p.prefix_mode) {
+            // the unnormalised partial (max m, sum l, accumulator) of this row
+            float* arow = p.pre_acc + idx * kD + c * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(arow + e) =
+                  make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                              __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+          } else {
+            __nv_bfloat16* orow = out + idx * kD + c * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                w[q] = pack_bf16(__uint_as_float(o[e + 2 * q]) * inv, __uint_as_float(o[e + 2 * q + 1]) * inv);
+              *reinterpret_cast<uint4*>(orow + e) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+        if (live && p.prefix_mode) p.pre_ml[idx] = make_float2(m, bar.bad_block ? -1.f : l);
+      }
     }
   }
+
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
@@ -555,6 +632,16 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
       !make_tmap(&tk, a.pool.k, kD, hkv, a.pool.num_blocks * kBlockSize, 64, 1, kBlockSize) ||
       !make_tmap(&tv, a.pool.v, kD, hkv, a.pool.num_blocks * kBlockSize, 64, 1, kBlockSize))
     return cudaErrorInvalidValue;
+  if (a.num_seqs > kMaxPrefixSeqs) return cudaErrorInvalidValue;
+  const int tq_tokens = kRowsTile / group;
+  // Two Q tiles per unit share every K/V tile and overlap one tile's softmax
+  // with the other's products, so a two-tile unit takes far less than twice a
+  // one-tile unit; one-tile units win only when all of them fit on the SMs at
+  // once.
+  const int64_t pairs = (a.num_tokens + 2 * tq_tokens - 1) / (2 * tq_tokens);
+  const int64_t budget = a.sm_budget > 0 ? a.sm_budget : device_sm_count();
+  const int q_tiles = a.q_tiles == 1 || a.q_tiles == 2 ? a.q_tiles : (2 * pairs * hkv > budget ? 2 : 1);
+  const int64_t units = (a.num_tokens + q_tiles * tq_tokens - 1) / (q_tiles * tq_tokens) + a.num_seqs;
   TcParams p;
   p.cu_q_lens = a.cu_q_lens;
   p.context_lens = a.context_lens;
@@ -566,21 +653,19 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   p.hkv = hkv;
   p.group = group;
   p.max_blocks = a.max_blocks_per_seq;
+  p.q_tiles = q_tiles;
   p.num_blocks = a.pool.num_blocks;
   p.scale_log2 = a.scale * kLog2e;
   p.d_status = a.d_status;
   p.prefix_mode = a.prefix_mode;
   p.pre_ml = static_cast<float2*>(a.pre_ml);
   p.pre_acc = static_cast<float*>(a.pre_acc);
-  const int tq_tokens = kRowsTile / group;
-  const int tiles = (a.num_tokens + tq_tokens - 1) / tq_tokens + a.num_seqs;  // upper bound
   const int smem = kSmemTc;
-  if (a.num_seqs > kMaxPrefixSeqs) return cudaErrorInvalidValue;
   cudaError_t err =
       cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles, hkv);
+  cfg.gridDim = dim3(static_cast<unsigned>(units * hkv));  // an upper bound; the rest exit
   cfg.blockDim = dim3(kThreadsTc);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

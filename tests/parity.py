@@ -88,13 +88,19 @@ def run_decode(w: W.Workload, db: DeviceBatch | None = None,
     return out, db
 
 
-def run_mixed(w: W.Workload, db: DeviceBatch | None = None, write: bool = True):
+def run_mixed(w: W.Workload, db: DeviceBatch | None = None, write: bool = True, units: int = 0):
+    """pa_mixed_step (units == 0) or pa_mixed_step_with_units with 1 or 2
+    query tiles per tensor-core prefill unit."""
     db = db or to_device(w)
     out = torch.empty_like(db.q)
-    pa.pa_mixed_step(out, db.q, db.cu_q_lens, db.context_lens, db.block_tables, db.k_pool,
-                     db.v_pool, w.scale, w.token_budget,
-                     k_new=db.k_new if write else None, v_new=db.v_new if write else None,
-                     slot_mapping=db.slot_mapping if write else None, d_status=db.status)
+    kw = dict(k_new=db.k_new if write else None, v_new=db.v_new if write else None,
+              slot_mapping=db.slot_mapping if write else None, d_status=db.status)
+    if units:
+        pa.pa_mixed_step_with_units(out, db.q, db.cu_q_lens, db.context_lens, db.block_tables,
+                                    db.k_pool, db.v_pool, w.scale, w.token_budget, units, **kw)
+    else:
+        pa.pa_mixed_step(out, db.q, db.cu_q_lens, db.context_lens, db.block_tables, db.k_pool,
+                         db.v_pool, w.scale, w.token_budget, **kw)
     torch.cuda.synchronize()
     return out, db
 

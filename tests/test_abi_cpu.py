@@ -108,6 +108,21 @@ def test_mixed_and_write_validation(lib):
     assert lib.pa_reshape_and_cache(ctypes.byref(pl), FAKE, FAKE, FAKE, 0, None, None) == abi.PA_OK
 
 
+def test_prefill_unit_size_is_an_argument(lib):
+    """pa_mixed_step_with_units takes 0, 1 or 2 query tiles per prefill unit;
+    anything else is rejected before any device work."""
+    pl = pool()
+    for bad in (-1, 3, 64):
+        rc = lib.pa_mixed_step_with_units(ctypes.byref(pl), FAKE, FAKE, FAKE, 2, 10, 8, FAKE, FAKE,
+                                          8, 0.1, 64, None, None, None, bad, FAKE, 1 << 40, None,
+                                          None)
+        assert rc == abi.PA_EINVAL
+    for ok in (0, 1, 2):  # valid unit sizes reach the workspace check
+        rc = lib.pa_mixed_step_with_units(ctypes.byref(pl), FAKE, FAKE, FAKE, 2, 10, 8, FAKE, FAKE,
+                                          8, 0.1, 64, None, None, None, ok, FAKE, 16, None, None)
+        assert rc == abi.PA_EWORKSPACE
+
+
 def test_decode_cta_count_is_an_argument(lib):
     """The CTA count is passed per call; the library has no setter for it."""
     assert not hasattr(lib, "pa_set_decode_ctas")

@@ -224,10 +224,13 @@ def test_chunked_prefill_example_on_gpu():
     compare(one_pass, r["one_pass"], torch.float32)
 
 
-def test_mixed_step_scaled_full():
-    """Config-4 structure with 4,096-token prompts, every row checked."""
+@pytest.mark.parametrize("units", [0, 1])
+def test_mixed_step_scaled_full(units):
+    """Config-4 structure with 4,096-token prompts, every row checked: the
+    library's choice (two query tiles per prefill unit at this size) and
+    one-tile units."""
     w = W.mixed_step(num_decode=16, decode_ctx=(64, 2048), prompt_len=4096)
-    out, db = run_mixed(w)
+    out, db = run_mixed(w, units=units)
     compare(out, oracle_out(w), torch.bfloat16)
     assert int(db.status.item()) == 0
 
@@ -275,36 +278,40 @@ def test_mixed_budget_rejected():
 # ------------------------------------------------------------------ tensor-core prefill
 
 
+@pytest.mark.parametrize("units", [1, 2])
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 8), (64, 8), (8, 2)])
-def test_prefill_tc_groups_and_ragged_chunks(hq, hkv):
+def test_prefill_tc_groups_and_ragged_chunks(hq, hkv, units):
     """bf16, head_dim 128 (the tcgen05 path): every GQA group size, chunks at
     offset 0 and at ragged offsets, chunk lengths that are not multiples of the
     tile, 2-token chunks, contexts spanning several 128-key tiles and partial
-    last blocks (slots past the context hold NaN)."""
+    last blocks (slots past the context hold NaN); units of one query tile and
+    of two (including two-tile units whose second tile is empty)."""
     ctx = [37, 300, 129, 1000, 2, 517, 64]
     ql = [37, 45, 2, 201, 2, 1, 17]
     w = W.paged_workload("tc", 21, ctx, ql, hq, hkv, 128, 300, torch.bfloat16, write_new=True)
-    out, db = run_mixed(w)
+    out, db = run_mixed(w, units=units)
     compare(out, oracle_out(w), torch.bfloat16)
     assert int(db.status.item()) == 0
 
 
-def test_prefill_tc_without_kv_write():
+@pytest.mark.parametrize("units", [1, 2])
+def test_prefill_tc_without_kv_write(units):
     """The cache already holds every token (no KV write in the step)."""
     ctx = [700, 260, 96]
     ql = [300, 260, 40]
     w = W.paged_workload("tc_nowrite", 22, ctx, ql, 32, 8, 128, 200, torch.bfloat16, write_new=False)
-    out, db = run_mixed(w, write=False)
+    out, db = run_mixed(w, write=False, units=units)
     compare(out, oracle_out(w), torch.bfloat16)
     assert int(db.status.item()) == 0
 
 
-def test_prefill_tc_chunked_equals_one_pass():
+@pytest.mark.parametrize("units", [1, 2])
+def test_prefill_tc_chunked_equals_one_pass(units):
     """A 1000-token prompt prefilled in chunks of 256 through the tensor-core
     path equals one pass, within the bf16 tolerance, and both match the oracle."""
     L, H, G = 1000, 8, 4
     w1 = W.paged_workload("onepass", 23, [L], [L], H * G, H, 128, 80, torch.bfloat16, write_new=True)
-    out1, _ = run_mixed(w1)
+    out1, _ = run_mixed(w1, units=units)
     ref = oracle_out(w1)
     compare(out1, ref, torch.bfloat16)
     db = to_device(w1)
@@ -314,10 +321,12 @@ def test_prefill_tc_chunked_equals_one_pass():
     for start in range(0, L, 256):
         end = min(start + 256, L)
         o = torch.empty(end - start, H * G, 128, dtype=torch.bfloat16, device="cuda")
-        pa.pa_mixed_step(o, db.q[start:end], torch.tensor([0, end - start], dtype=torch.int32).cuda(),
-                         torch.tensor([end], dtype=torch.int32).cuda(), db.block_tables, db.k_pool,
-                         db.v_pool, w1.scale, 2048, k_new=db.k_new[start:end],
-                         v_new=db.v_new[start:end], slot_mapping=db.slot_mapping[start:end])
+        pa.pa_mixed_step_with_units(o, db.q[start:end],
+                                    torch.tensor([0, end - start], dtype=torch.int32).cuda(),
+                                    torch.tensor([end], dtype=torch.int32).cuda(), db.block_tables,
+                                    db.k_pool, db.v_pool, w1.scale, 2048, units,
+                                    k_new=db.k_new[start:end], v_new=db.v_new[start:end],
+                                    slot_mapping=db.slot_mapping[start:end])
         outs.append(o)
     chunked = torch.cat(outs)
     compare(chunked, ref, torch.bfloat16)
