@@ -24,13 +24,15 @@
 //    alternate: while the softmax of one tile runs, the tensor pipe works on
 //    the other's products, and S_x(j+1) follows P_x(j) V(j) in the pipe.
 //  * Warps 2-5 (Q tile 0) and 6-9 (Q tile 1) hold one thread per query row.
-//    Each reads its row of S from TMEM and writes P = 2^(s - m) as bf16 pairs
-//    over the first 64 columns it read, m being its running max in the log2
-//    domain. The max moves only when a score exceeds it by more than 8 (lazy
-//    rescaling), and the row sum bounds every weight: while the sum stays at
-//    or below 2^8 no score passed m + 8, so the tile needs no max pass. Only
-//    otherwise (and on the first tile) is the row's max taken and P redone
-//    with it, O rescaled in TMEM when the max moved. Masked keys get weight 0.
+//    Each reads its row of S from TMEM, 64 keys at a time, and writes
+//    P = 2^(s - m) of those keys as bf16 pairs over scores it has read, m
+//    being its running max in the log2 domain. The max moves only when a
+//    score exceeds it by more than 8 (lazy rescaling), and a sum bounds every
+//    weight in it: while a half's sum stays at or below 2^8 no score of it
+//    passed m + 8, so the tile needs no max pass. Only otherwise (and on the
+//    first tile) is the max of the scores still in TMEM taken and the half
+//    redone with it (P of the first half, already stored, rescaled in place),
+//    O rescaled in TMEM when the max moved. Masked keys get weight 0.
 //  * On the last key tile the rows of Q tile 0 zero the value rows that lie
 //    past the context or past the loaded blocks, before P_0 goes to the MMA,
 //    so stale or NaN slots never reach the result.
@@ -431,66 +433,57 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // rows past the unit keep m = +inf: every weight is 0 and nothing moves
     float m = live ? -INFINITY : INFINITY, l = 0.f;
     bool ok = x < nq;
-    // P = 2^(s - mm) of this row's 128 keys (0 past the row's position) into
-    // pk; returns the row sum
-    auto weights = [&](float mm, bool full, int key0, uint32_t (&pk)[64]) -> float {
+    // P = 2^(s - mm) of the 64 keys of half h of the tile (0 past the row's
+    // position) into pk; returns their sum
+    auto weights = [&](int h, float mm, bool full, int key0, uint32_t (&pk)[32]) -> float {
       float2 acc[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+      uint32_t raw[2][32];
+      tc::tmem_ld32(scol + h * 64, raw[0]);
+      tc::tmem_ld32(scol + h * 64 + 32, raw[1]);
+      tc::tmem_wait_ld();
       if (full) {
         const float2 c2 = make_float2(sl2, sl2);
         const float2 nm = make_float2(-mm, -mm);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t raw[2][32];
-          tc::tmem_ld32(scol + h * 64, raw[0]);
-          tc::tmem_ld32(scol + h * 64 + 32, raw[1]);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float2 sv = make_float2(__uint_as_float(raw[c >> 4][(2 * c) & 31]),
-                                          __uint_as_float(raw[c >> 4][(2 * c + 1) & 31]));
-            const float2 t = __ffma2_rn(sv, c2, nm);
-            const float2 w = make_float2(ex2(t.x), ex2(t.y));
-            acc[c & 3] = __fadd2_rn(acc[c & 3], w);
-            pk[h * 32 + c] = pack_bf16(w.x, w.y);
-          }
+        for (int c = 0; c < 32; ++c) {
+          const float2 sv = make_float2(__uint_as_float(raw[c >> 4][(2 * c) & 31]),
+                                        __uint_as_float(raw[c >> 4][(2 * c + 1) & 31]));
+          const float2 t = __ffma2_rn(sv, c2, nm);
+          const float2 w = make_float2(ex2(t.x), ex2(t.y));
+          acc[c & 3] = __fadd2_rn(acc[c & 3], w);
+          pk[c] = pack_bf16(w.x, w.y);
         }
       } else {
         // tiles that cross a row's position: keys past it get weight 0
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t raw[2][32];
-          tc::tmem_ld32(scol + h * 64, raw[0]);
-          tc::tmem_ld32(scol + h * 64 + 32, raw[1]);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int key = key0 + h * 64 + 2 * c;
-            const float a = key <= pos ? __uint_as_float(raw[c >> 4][(2 * c) & 31]) * sl2 : -INFINITY;
-            const float b = key + 1 <= pos ? __uint_as_float(raw[c >> 4][(2 * c + 1) & 31]) * sl2 : -INFINITY;
-            const float2 w = make_float2(a == -INFINITY ? 0.f : ex2(a - mm), b == -INFINITY ? 0.f : ex2(b - mm));
-            acc[c & 3] = __fadd2_rn(acc[c & 3], w);
-            pk[h * 32 + c] = pack_bf16(w.x, w.y);
-          }
+        for (int c = 0; c < 32; ++c) {
+          const int key = key0 + h * 64 + 2 * c;
+          const float a = key <= pos ? __uint_as_float(raw[c >> 4][(2 * c) & 31]) * sl2 : -INFINITY;
+          const float b = key + 1 <= pos ? __uint_as_float(raw[c >> 4][(2 * c + 1) & 31]) * sl2 : -INFINITY;
+          const float2 w = make_float2(a == -INFINITY ? 0.f : ex2(a - mm), b == -INFINITY ? 0.f : ex2(b - mm));
+          acc[c & 3] = __fadd2_rn(acc[c & 3], w);
+          pk[c] = pack_bf16(w.x, w.y);
         }
       }
       return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
     };
-    // the row's largest score of the tile in the log2 domain (-inf if none)
-    auto row_max = [&](int key0) -> float {
+    // the row's largest score among the tile's keys from column c0 on (0 or
+    // 32; the columns before it hold P already) in the log2 domain, -inf if none
+    auto row_max = [&](int key0, int c0) -> float {
       float mp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t raw[2][32];
-        tc::tmem_ld32(scol + h * 64, raw[0]);
-        tc::tmem_ld32(scol + h * 64 + 32, raw[1]);
+      for (int q = 0; q < 4; ++q) {
+        if (q * 32 < c0) continue;  // warp-uniform
+        uint32_t raw[32];
+        tc::tmem_ld32(scol + q * 32, raw);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const float v = key0 + h * 64 + e <= pos ? __uint_as_float(raw[e >> 5][e & 31]) * sl2 : -INFINITY;
+        for (int e = 0; e < 32; ++e) {
+          const float v = key0 + q * 32 + e <= pos ? __uint_as_float(raw[e]) * sl2 : -INFINITY;
           mp[e & 7] = fmaxf(mp[e & 7], v);
         }
       }
@@ -504,22 +497,44 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int key0 = j * kKeysTile;
       // every row of the tile sees every key of this tile: no mask
       const bool full = key0 + kKeysTile - 1 <= pos_first && sl2 > 0.f;
-      uint32_t pk[64];
-      float rs, alpha = 1.f;
+      float rs = 0.f, alpha = 1.f;
       bool warp_moved = false;
-      // P with the running max; a weight above 2^8 is possible only if the
-      // sum is, and then the row's max is taken and P redone if it moved
+      // Each half's P goes to TMEM (keys 2c, 2c + 1 of the half in column
+      // 32 h + c, over scores already read) as soon as it is final. P uses
+      // the running max; a weight above 2^8 is possible only if the half's sum
+      // is, and then the max of the scores still in TMEM is taken: for half 1
+      // every key of half 0 is known to lie within 8 of the old max, so that
+      // max decides. When it moves, half 0's stored P (half 1 only) is
+      // rescaled in place and the half redone.
 #pragma unroll 1
-      for (int pass = 0;; ++pass) {
-        rs = weights(m, full, key0, pk);
-        if (pass > 0 || !__any_sync(0xffffffffu, !(rs <= 256.f))) break;
-        const float mx = row_max(key0);
-        const bool need = mx > m + 8.f;
-        warp_moved = __any_sync(0xffffffffu, need);
-        if (!warp_moved) break;
-        const float mn = need ? mx : m;
-        alpha = (m == -INFINITY) ? 0.f : (need ? ex2(m - mn) : 1.f);
-        m = mn;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+        float rh = weights(h, m, full, key0, pk);
+        if (__any_sync(0xffffffffu, !(rh <= 256.f))) {
+          const float mx = row_max(key0, h * 32);
+          const bool need = mx > m + 8.f;
+          if (__any_sync(0xffffffffu, need)) {
+            warp_moved = true;
+            const float mn = need ? mx : m;
+            const float a = (m == -INFINITY) ? 0.f : (need ? ex2(m - mn) : 1.f);
+            m = mn;
+            alpha *= a;
+            if (h == 1) {
+              uint32_t p0[32];
+              tc::tmem_wait_st();
+              tc::tmem_ld32(scol, p0);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                p0[c] = pack_bf16(__uint_as_float(p0[c] << 16) * a, __uint_as_float(p0[c] & 0xffff0000u) * a);
+              tc::tmem_st32(scol, p0);
+              rs *= a;
+            }
+            rh = weights(h, m, full, key0, pk);
+          }
+        }
+        rs += rh;
+        tc::tmem_st32(scol + h * 32, pk);
       }
       l = l * alpha + rs;
       // O holds key tiles 0 .. j-1 once P(j-1) V(j-1) is complete: rescale
@@ -538,8 +553,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tc::tmem_st32(ocol + c * 32, o);
         }
       }
-      // P (bf16 pairs, keys 2c and 2c + 1 in column c) over the first 64 S columns
-      tc::tmem_st64(scol, pk);
       tc::tmem_wait_st();
       // last tile: Q tile 0's rows zero the value rows no key of this unit may
       // use (thread r: key row r, both 64-column halves) before P_0 goes to
