@@ -42,6 +42,7 @@
 //    wait (bounded) for their copies and MMAs in flight, and the CTA releases
 //    its TMEM and leaves.
 #include <cuda.h>
+#include <algorithm>
 #include <cuda_runtime.h>
 
 #include "pa_common.cuh"
@@ -658,7 +659,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   const int64_t pairs = (a.num_tokens + 2 * tq_tokens - 1) / (2 * tq_tokens);
   const int64_t budget = a.sm_budget > 0 ? a.sm_budget : device_sm_count();
   const int q_tiles = a.q_tiles == 1 || a.q_tiles == 2 ? a.q_tiles : (2 * pairs * hkv > budget ? 2 : 1);
-  const int64_t units = (a.num_tokens + q_tiles * tq_tokens - 1) / (q_tiles * tq_tokens) + a.num_seqs;
+  // at most sum(ceil(q_len / T)) <= num_tokens / T + (sequences with units):
+  // every prefill chunk has two rows or more (prefix groups one or more)
+  const int64_t with_units = a.prefix_mode ? a.num_seqs : std::min<int64_t>(a.num_seqs, a.num_tokens / 2);
+  const int64_t units = (a.num_tokens + q_tiles * tq_tokens - 1) / (q_tiles * tq_tokens) + with_units;
   TcParams p;
   p.cu_q_lens = a.cu_q_lens;
   p.context_lens = a.context_lens;
