@@ -332,6 +332,44 @@ def test_prefill_tc_chunked_equals_one_pass(units):
     compare(chunked, ref, torch.bfloat16)
 
 
+@pytest.mark.parametrize("units", [1, 2])
+def test_prefill_tc_running_max_jumps(units):
+    """Scores that jump far past the lazy-rescale threshold (8 in the log2
+    domain) inside later key tiles, for one query head of a group only, so a
+    warp holds rows whose running max moves and rows whose max stays: a jump
+    in the second 64-key half of a tile (the first half's P is already in
+    TMEM and is rescaled in place), a larger one in the first half of the
+    next tile, and one among the chunk's own keys; both unit sizes."""
+    hq, hkv, G = 32, 8, 4
+    w = W.paged_workload("jumps", 31, [700, 420], [180, 64], hq, hkv, 128, 200, torch.bfloat16,
+                         write_new=True)
+    q, k_pool, k_new = w.q.clone(), w.k_pool.clone(), w.k_new.clone()
+    cu = w.cu_q_lens.tolist()
+    rng = np.random.default_rng(7)
+    # (first, last + 1, scale) of planted cached keys per sequence: sequence 0
+    # jumps in keys 192-255 of key tile 1, then again in keys 256-319 of
+    # tile 2; sequence 1 in keys 128-191 of tile 1
+    plants = {0: [(200, 205, 4.0), (300, 303, 6.0)], 1: [(150, 153, 3.0)]}
+    for s_i, spans in plants.items():
+        g = s_i  # KV head whose query head g * G sees the planted keys
+        u = torch.from_numpy(rng.standard_normal(128)).to(torch.bfloat16)
+        t0, t1 = cu[s_i], cu[s_i + 1]
+        q[t0:t1, g * G] = u  # one query head of the group, every row of the chunk
+        first_new = int(w.context_lens[s_i]) - (t1 - t0)
+        for lo, hi, c in spans:
+            for pos in range(lo, hi):
+                assert pos < first_new  # a cached key, in the pool
+                blk = int(w.block_tables[s_i, pos // 16])
+                k_pool[blk, pos % 16, g] = (c * u.float()).to(torch.bfloat16)
+        # one planted key among the chunk's own tokens, written by the step:
+        # for sequence 1 it jumps again inside keys 320-383 of tile 2
+        k_new[t0 + 5, g] = (5.0 * u.float()).to(torch.bfloat16)
+    w.q, w.k_pool, w.k_new = q, k_pool, k_new
+    out, db = run_mixed(w, units=units)
+    compare(out, oracle_out(w), torch.bfloat16)
+    assert int(db.status.item()) == 0
+
+
 def test_gather_probe_runs_and_flags_bad_blocks():
     # the measurement aid of include/pa_probe.h: no output, only a status
     k = torch.zeros(64, 16, 8, 128, dtype=torch.bfloat16, device="cuda")
