@@ -407,6 +407,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         "gpu_launches": launches_per_step * args.steps,
         "pages_context": PAGES_CONTEXT,
         "clocks": clk,
+        "build": build_record(),
     }
     if mixed is not None:
         res["mixed_step"] = mixed
@@ -677,6 +678,13 @@ def run_decode_workload(name: str, w, dev, stream, reps: int = 30, groups=None) 
     del d, out, ws
     torch.cuda.empty_cache()
     return res
+
+
+def build_record() -> dict:
+    """Whether the libpa.so this run loaded matches these sources and this
+    machine (the build is redone on any other)."""
+    from paged_kv_cache_176_gb300.build import build_record as rec
+    return rec()
 
 
 def run_mixed(args, dev, stream) -> dict:

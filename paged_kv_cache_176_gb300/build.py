@@ -15,11 +15,13 @@ from __future__ import annotations
 import concurrent.futures as fut
 import glob
 import hashlib
+import json
 import os
 import platform
 import shutil
 import subprocess
 import sys
+import time
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
@@ -27,6 +29,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
 PROBE_LIB = os.path.join(HERE, "libpa_probe.so")
 STAMP = os.path.join(BUILD, "stamp")
+RECORD = os.path.join(BUILD, "record.json")  # what the last compilation built, where and when
 ROOT = os.path.dirname(HERE)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
@@ -63,8 +66,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     stamp = _stamp(extra_flags)
     if (not force and os.path.exists(LIB) and os.path.exists(PROBE_LIB) and os.path.exists(STAMP)
             and open(STAMP).read().strip() == stamp):
-        if verbose:
-            sys.stderr.write("libpa: up to date\n")
+        sys.stderr.write(f"libpa: reusing the build of these sources on {platform.machine()} "
+                         f"(stamp {stamp[:16]})\n")
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     lib_srcs, probe_srcs = _sources()
@@ -93,9 +96,26 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         os.replace(tmp, out)
     with open(STAMP, "w") as f:
         f.write(stamp + "\n")
+    with open(RECORD, "w") as f:
+        json.dump({"stamp": stamp[:16], "machine": platform.machine(), "units": len(srcs),
+                   "compiled_unix_s": round(time.time(), 1)}, f)
     sys.stderr.write(f"libpa: compiled {len(srcs)} translation units for sm_103a "
                      f"on {platform.machine()}\n")
     return LIB
+
+
+def build_record() -> dict:
+    """Whether libpa.so was built from these sources on this machine, and when
+    it was compiled (for run records: a library carried over from another
+    machine or older sources shows here)."""
+    cur = _stamp(())
+    rec = {"stamp": cur[:16], "machine": platform.machine(), "matches_sources": False}
+    if os.path.exists(STAMP):
+        rec["matches_sources"] = open(STAMP).read().strip() == cur
+    if os.path.exists(RECORD):
+        with open(RECORD) as f:
+            rec["last_compile"] = json.load(f)
+    return rec
 
 
 if __name__ == "__main__":
