@@ -687,12 +687,16 @@ def build_record() -> dict:
     return rec()
 
 
+MIXED_WORKLOAD: list = []
+
+
 def run_mixed(args, dev, stream) -> dict:
     import torch
     import paged_kv_cache_176_gb300 as pa
     from paged_kv_cache_176_gb300 import workloads as W
 
     w = W.mixed_step(seed=args.seed)
+    MIXED_WORKLOAD[:] = [w]  # kept for the oracle sample after the GPU legs
     work = mixed_work(w)
     with torch.cuda.stream(stream):
         d = {k: getattr(w, k).to(dev) for k in ("k_pool", "v_pool", "q", "cu_q_lens",
@@ -917,6 +921,37 @@ def torch_tensor_bool(a):
     return torch.from_numpy(a.astype(bool))
 
 
+def mixed_cpu_baseline(w, seed: int) -> dict:
+    """The fp64 oracle, as it stands, on a bounded sample of the mixed step:
+    every decode row and 8 seeded rows of each prefill chunk (all heads, the
+    step's KV write included); its FLOP rate over those rows, counted as the
+    GPU arm counts the prefill (4·d per unmasked query-key pair)."""
+    import numpy as np
+    import oracle
+    cu = w.cu_q_lens.tolist()
+    ctx = w.context_lens.tolist()
+    rng = np.random.default_rng(seed + 11)
+    mask = np.zeros(w.num_tokens, dtype=np.uint8)
+    flops = 0
+    for s in range(w.num_seqs):
+        ql = cu[s + 1] - cu[s]
+        rows = [cu[s]] if ql == 1 else sorted(rng.choice(np.arange(cu[s], cu[s + 1]), 8, replace=False))
+        for r in rows:
+            mask[r] = 1
+            keys = ctx[s] - ql + (r - cu[s]) + 1
+            flops += 4 * w.num_q_heads * w.head_dim * keys
+    cores = os.cpu_count() or 1
+    lib = oracle.load()
+    t0 = time.perf_counter()
+    oracle.workload_attention(w, row_mask=mask, num_threads=cores, lib=lib)
+    secs = time.perf_counter() - t0
+    return {"value": round(flops / secs / 1e9, 2), "unit": "GFLOP/s", "cores": cores,
+            "kind": "oracle", "rows": int(mask.sum()), "flops": int(flops),
+            "seconds": round(secs, 2),
+            "sample": f"every decode row and 8 seeded rows of each prefill chunk "
+                      f"({int(mask.sum())} of {w.num_tokens} query rows, all heads)"}
+
+
 def cpu_baseline(seed: int, budget_s: float) -> dict:
     """Oracle throughput on whole passes over the decode batch, repeated until
     about ``budget_s`` seconds of CPU work."""
@@ -1022,6 +1057,8 @@ def main() -> None:
         res = run_gpu(args, rank, world)
         if res is not None and rank == 0 and not args.skip_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(args.seed, args.cpu_budget_s)
+            if "mixed_step" in res and MIXED_WORKLOAD:
+                res["mixed_step"]["cpu_baseline"] = mixed_cpu_baseline(MIXED_WORKLOAD[0], args.seed)
     if world > 1:
         import torch.distributed as tdist
         tdist.barrier()
