@@ -370,6 +370,35 @@ def test_prefill_tc_running_max_jumps(units):
     assert int(db.status.item()) == 0
 
 
+@pytest.mark.parametrize("hq,hkv,d,dtype,units", [(64, 8, 128, torch.bfloat16, 1),
+                                                   (64, 8, 128, torch.bfloat16, 2),
+                                                   (8, 2, 64, torch.float32, 0)])
+def test_prefill_bad_block_and_length_zeroed(hq, hkv, d, dtype, units):
+    """A prefill chunk whose first block-table entry is out of range (every
+    unit of it reads that block) and a chunk longer than its context: both
+    flagged in the status word, their rows zero; the decode rows and the
+    other chunk of the step still match the oracle. Tensor-core prefill with
+    one- and two-tile units, and the CUDA-core prefill."""
+    ctx = [300, 700, 200, 90, 40]
+    ql = [1, 150, 60, 1, 33]
+    w = W.paged_workload("bad_pf", 41, ctx, ql, hq, hkv, d, 160, dtype, write_new=True)
+    ref = oracle_out(w)  # with the valid tables and lengths
+    db = to_device(w)
+    db.block_tables[1, 0] = int(w.k_pool.shape[0]) + 5  # sequence 1: bad first block
+    db.context_lens[4] = 20  # sequence 4: 33 rows over a context of 20
+    out, db = run_mixed(w, db=db, units=units)
+    st = int(db.status.item())
+    assert st & pa.abi.PA_STATUS_BAD_BLOCK and st & pa.abi.PA_STATUS_BAD_LENGTH
+    cu = w.cu_q_lens.tolist()
+    bad = np.zeros(w.num_tokens, dtype=bool)
+    for s in (1, 4):
+        bad[cu[s]:cu[s + 1]] = True
+    got = out.float().cpu()
+    assert torch.count_nonzero(got[torch.from_numpy(bad)]) == 0
+    good = np.nonzero(~bad)[0]
+    compare(out, ref, dtype, rows=good)
+
+
 def test_gather_probe_runs_and_flags_bad_blocks():
     # the measurement aid of include/pa_probe.h: no output, only a status
     k = torch.zeros(64, 16, 8, 128, dtype=torch.bfloat16, device="cuda")
