@@ -259,7 +259,10 @@ PA_API size_t pa_mixed_workspace_size(int num_seqs, int num_tokens, int num_q_he
  * num_seqs: P >= 1024 and num_seqs <= P / 12), the decode rows run on 48 SMs
  * and the prefill beside them on the other SMs (a programmatic dependent
  * launch on the same stream; neither kernel waits for the other); otherwise
- * the prefill runs first on all SMs, then the decode.
+ * the prefill runs first on all SMs, then the decode. The tensor-core prefill
+ * serves two 128-row query tiles from each K/V tile when one-tile units would
+ * not all fit on the SMs it gets at once, else one
+ * (pa_mixed_step_with_units fixes the choice).
  *
  *  cu_q_lens     device int32 [num_seqs + 1], cu_q_lens[0] = 0, non-decreasing,
  *                cu_q_lens[num_seqs] = num_tokens
