@@ -404,10 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
   };
   // the first stages are issued from the global table at once, so their
-  // copies are in flight while the CTA stages the rest of its table slice
-  if (tid == 0) {
-    for (int u = 0; u < min(static_cast<int64_t>(L.stages), n_units); ++u) issue(u, u, true);
-  }
+  // copies are in flight while the CTA stages the rest of its table slice;
+  // one thread each, so their table lookups overlap
+  if (tid < min(static_cast<int64_t>(L.stages), n_units)) issue(tid, tid, true);
 
 
   // stage this CTA's slice of the block tables (first kTableCache blocks)
