@@ -91,6 +91,7 @@ class ClockSampler:
         self.interval_ms = interval_ms
         self.proc = None
         self.lines: list[str] = []
+        self.skip = 0  # leading lines printed before the measured region
         self._t = None
 
     def start(self):
@@ -109,6 +110,15 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def wait_first(self, limit_s: float = 3.0) -> "ClockSampler":
+        """Block until nvidia-smi has printed its first sample (at most
+        ``limit_s``), so that a short timed region is not spent while the
+        sampler is still starting."""
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < limit_s:
+            time.sleep(0.005)
+        return self
+
     def stop(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -121,7 +131,7 @@ class ClockSampler:
             self._t.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in self.lines[self.skip:]:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -219,7 +229,8 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     torch.cuda.synchronize(dev)
     # events around every pa_decode call, in batches of 200 calls, until at
     # least 1 s of calls has run (whatever --steps is); clocks sampled meanwhile
-    roof_clocks = ClockSampler(dev.index).start()
+    roof_clocks = ClockSampler(dev.index).start().wait_first()
+    roof_clocks.skip = len(roof_clocks.lines)
     times, t_start = [], time.perf_counter()
     while time.perf_counter() - t_start < 1.0 or len(times) < 200:
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -241,7 +252,8 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         import torch.distributed as tdist
         tdist.barrier()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(dev.index).start()
+    clocks = ClockSampler(dev.index).start().wait_first()
+    clocks.skip = len(clocks.lines)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -250,6 +262,11 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     t1.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
+    if not clk.get("samples"):
+        # a timed region shorter than one sampling interval: report the
+        # decode-call window's record (the same calls, >= 1 s, just before)
+        clk = dict(roof_clk, source="decode-call window just before the timed region "
+                   "(the timed region was shorter than one sampling interval)")
     ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, dev)
 
     # end to end through the public API with host buffers: every step copies
@@ -442,6 +459,13 @@ def run_extra(args, dev, stream) -> list:
     out.append(run_decode_workload(SHARED_PREFIX_WORKLOAD + "; pa_decode_cascade, one group "
                                    f"sharing {plen} prefix tokens", w, dev, stream,
                                    groups=([0, w.num_seqs], [plen])))
+    R, rep = w.info["num_requests"], w.info["replies"]
+    prompt_full = (w.info["prompt_len"] // 16) * 16
+    out.append(run_decode_workload(
+        SHARED_PREFIX_WORKLOAD + f"; pa_decode_cascade_nested, one group sharing {plen} prefix "
+        f"tokens and {R} sibling groups (a request's {rep} replies) sharing {prompt_full} prompt "
+        "tokens", w, dev, stream, groups=([0, w.num_seqs], [plen]),
+        siblings=([r * rep for r in range(R + 1)], [prompt_full] * R)))
     del w
     out.append(run_cow_step(args, dev, stream))
     return out
@@ -604,14 +628,17 @@ def gather_ceiling(w, kp, vp, dev, stream, stages: int = 3, reps: int = 50) -> d
             "frac_of_copy_peak": round(gbs / peaks()["hbm_gbs"], 4), "stages": stages}
 
 
-def run_decode_workload(name: str, w, dev, stream, reps: int = 30, groups=None) -> dict:
+def run_decode_workload(name: str, w, dev, stream, reps: int = 30, groups=None,
+                        siblings=None) -> dict:
     """One decode step (KV write when the workload has one, then pa_decode, or
-    pa_decode_cascade when ``groups`` = (cu_groups, prefix_lens) is given) on
-    another workload, timed with CUDA events on its stream; GB/s over the
-    logical K/V bytes (every sequence's context) and over the unique bytes
-    (each physical block's filled slots counted once). A cascade also reports
-    GB/s over the bytes it has to read: each group's prefix once, plus every
-    sequence's tokens after its prefix."""
+    pa_decode_cascade when ``groups`` = (cu_groups, prefix_lens) is given, or
+    pa_decode_cascade_nested when ``siblings`` = (cu_siblings, sibling_lens)
+    is given as well) on another workload, timed with CUDA events on its
+    stream; GB/s over the logical K/V bytes (every sequence's context) and over
+    the unique bytes (each physical block's filled slots counted once). A
+    cascade also reports GB/s over the bytes it has to read: each group's
+    prefix once, each sibling entry's shared tokens after that prefix once, and
+    every sequence's tokens after what it shares."""
     import torch
     import paged_kv_cache_176_gb300 as pa
 
@@ -627,20 +654,42 @@ def run_decode_workload(name: str, w, dev, stream, reps: int = 30, groups=None) 
     cascade_bytes = None
     if groups is not None:
         cu, pl = groups
-        cascade_bytes = sum(pl) * tok + sum(
-            (ctx[s] - pl[g]) * tok for g in range(len(pl)) for s in range(cu[g], cu[g + 1]))
-        cascade_bytes += sum(ctx[s] for s in range(cu[-1], len(ctx))) * tok
+        skip = [0] * len(ctx)  # first-level prefix tokens of each sequence
+        for g in range(len(pl)):
+            for s in range(cu[g], cu[g + 1]):
+                skip[s] = pl[g]
+        own = [ctx[s] - skip[s] for s in range(len(ctx))]
+        cascade_bytes = sum(pl) * tok
+        if siblings is not None:
+            # entries of 16 / G members on the tensor-core decode (8 KV heads, bf16)
+            G = w.num_q_heads // w.num_kv_heads
+            per = 16 // G if (w.num_kv_heads == 8 and w.k_pool.element_size() == 2
+                              and w.head_dim <= 128) else 1
+            scu, sl = siblings
+            for j in range(len(sl)):
+                for a in range(scu[j], scu[j + 1], per):
+                    cascade_bytes += (sl[j] - skip[a]) * tok
+                for s in range(scu[j], scu[j + 1]):
+                    own[s] = ctx[s] - sl[j]
+        cascade_bytes += sum(own) * tok
     with torch.cuda.stream(stream):
         d = {k: (None if getattr(w, k) is None else getattr(w, k).to(dev))
              for k in ("k_pool", "v_pool", "q", "context_lens", "block_tables", "k_new", "v_new",
                        "slot_mapping")}
         out = torch.empty_like(d["q"])
-        size = pa.pa_decode_cascade_workspace_size if groups else pa.pa_decode_workspace_size
-        ws = torch.empty(size(w.num_seqs, w.num_q_heads, w.head_dim, w.max_blocks_per_seq),
-                         dtype=torch.uint8, device=dev)
+        if siblings is not None:
+            nbytes = pa.pa_decode_cascade_nested_workspace_size(
+                w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_blocks_per_seq)
+        else:
+            size = pa.pa_decode_cascade_workspace_size if groups else pa.pa_decode_workspace_size
+            nbytes = size(w.num_seqs, w.num_q_heads, w.head_dim, w.max_blocks_per_seq)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         if groups is not None:
             d_cu = torch.tensor(groups[0], dtype=torch.int32, device=dev)
             d_pl = torch.tensor(groups[1], dtype=torch.int32, device=dev)
+        if siblings is not None:
+            d_scu = torch.tensor(siblings[0], dtype=torch.int32, device=dev)
+            d_sl = torch.tensor(siblings[1], dtype=torch.int32, device=dev)
 
     def step():
         if d["slot_mapping"] is not None:
@@ -649,10 +698,14 @@ def run_decode_workload(name: str, w, dev, stream, reps: int = 30, groups=None) 
         if groups is None:
             pa.pa_decode(out, d["q"], d["k_pool"], d["v_pool"], d["block_tables"],
                          d["context_lens"], w.scale, workspace=ws, stream=stream)
-        else:
+        elif siblings is None:
             pa.pa_decode_cascade(out, d["q"], d["k_pool"], d["v_pool"], d["block_tables"],
                                  d["context_lens"], d_cu, d_pl, w.scale, workspace=ws,
                                  stream=stream)
+        else:
+            pa.pa_decode_cascade_nested(out, d["q"], d["k_pool"], d["v_pool"],
+                                        d["block_tables"], d["context_lens"], d_cu, d_pl, d_scu,
+                                        d_sl, w.scale, workspace=ws, stream=stream)
 
     for _ in range(5):
         step()

@@ -219,6 +219,60 @@ PA_API int pa_decode_cascade(const pa_kv_pool* pool, void* out, const void* q, i
                              void* workspace, size_t workspace_bytes, int* d_status, void* stream);
 
 /*
+ * Two-level cascade decode: pa_decode_cascade's groups (first level: a
+ * prefix shared by many sequences, e.g. a system prompt, read once per group
+ * by the tensor-core prefix pass) plus sibling groups (second level: a few
+ * sequences that share a longer prefix, e.g. the replies of one request,
+ * which share all of its prompt's full pages; "C13 L2 serving", parallel
+ * sampling paragraph). A sibling group's shared blocks after the first-level
+ * prefix are read once per entry of up to 16 / (num_q_heads / num_kv_heads)
+ * members: the decode kernel puts the members' query rows together in one
+ * 16-row tensor-core tile, so each such block is loaded and multiplied once
+ * for all of them. Each member's own blocks are read for that member only (the
+ * other rows of the tile are masked). The result is the same attention as
+ * pa_decode, up to floating-point summation order.
+ *
+ * Sibling groups: sequences cu_siblings[j] .. cu_siblings[j+1]-1 form
+ * sibling group j; their first sibling_lens[j] tokens (a multiple of 16, at
+ * most each member's context, at least the member's first-level prefix) are
+ * held by the same physical blocks, read through the first row of each entry
+ * (entries are consecutive runs of members from cu_siblings[j]); the caller
+ * guarantees the block equality (not checked). Members of one sibling group
+ * must have the same first-level prefix length. cu_siblings is non-decreasing
+ * within [0, num_seqs]. num_sibling_groups == 0 gives pa_decode_cascade (with
+ * this call's workspace); num_groups == 0 leaves out the first level.
+ *
+ * The sibling entries run on the tensor-core decode path (bf16, head_dim 64 or
+ * 128, 8 KV heads); with fewer KV heads the decode walks every sequence on
+ * its own (same result, no second-level saving).
+ *
+ * Errors: a sibling length that is not whole blocks, is shorter than the
+ * member's first-level prefix or longer than its context, or a member whose
+ * entry's first member has lengths that cannot hold the shared blocks, sets
+ * PA_STATUS_BAD_LENGTH in *d_status and zeroes that member's output row (a
+ * bad first member of an entry makes every member of the entry bad).
+ *
+ *  cu_siblings    device int32 [num_sibling_groups + 1]
+ *  sibling_lens   device int32 [num_sibling_groups], tokens
+ *  num_ctas       persistent decode CTAs as in pa_decode_cascade_with_ctas
+ *                 (0: the default); the workspace depends on it
+ *  other arguments as pa_decode_cascade; workspace >=
+ *  pa_decode_cascade_nested_workspace_size(num_seqs, num_q_heads,
+ *  num_kv_heads, head_dim, max_blocks_per_seq, num_ctas)
+ */
+PA_API size_t pa_decode_cascade_nested_workspace_size(int num_seqs, int num_q_heads,
+                                                      int num_kv_heads, int head_dim,
+                                                      int max_blocks_per_seq, int num_ctas);
+PA_API int pa_decode_cascade_nested(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+                                    int num_q_heads, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens,
+                                    const int32_t* cu_groups, const int32_t* prefix_lens,
+                                    int num_groups, const int32_t* cu_siblings,
+                                    const int32_t* sibling_lens, int num_sibling_groups,
+                                    float scale, int num_ctas, void* workspace,
+                                    size_t workspace_bytes, int* d_status, void* stream);
+
+/*
  * pa_decode and pa_decode_cascade with an explicit number of persistent
  * decode CTAs instead of the default of one per SM of the current device
  * (num_ctas == 0 keeps the default; values above 1024 are clamped; negative

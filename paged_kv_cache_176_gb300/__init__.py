@@ -15,6 +15,8 @@ from .abi import (  # noqa: F401
     pa_decode_with_ctas,
     pa_mixed_step_with_units,
     pa_decode_cascade_with_ctas,
+    pa_decode_cascade_nested,
+    pa_decode_cascade_nested_workspace_size,
     pa_strerror,
     pa_version,
 )
@@ -30,6 +32,8 @@ __all__ = [
     "pa_decode_with_ctas",
     "pa_mixed_step_with_units",
     "pa_decode_cascade_with_ctas",
+    "pa_decode_cascade_nested",
+    "pa_decode_cascade_nested_workspace_size",
     "pa_strerror",
     "pa_version",
     "PagedAttentionError",

@@ -95,6 +95,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_decode_cascade_with_ctas.restype = I
         lib.pa_decode_cascade_with_ctas.argtypes = [PP, P, P, I, I, P, I, P, P, P, I, F, I, P, SZ, P,
                                                     P]
+        lib.pa_decode_cascade_nested_workspace_size.restype = SZ
+        lib.pa_decode_cascade_nested_workspace_size.argtypes = [I, I, I, I, I, I]
+        lib.pa_decode_cascade_nested.restype = I
+        lib.pa_decode_cascade_nested.argtypes = [PP, P, P, I, I, P, I, P, P, P, I, P, P, I, F, I,
+                                                 P, SZ, P, P]
         _lib = lib
         return lib
 
@@ -281,6 +286,47 @@ def pa_decode_cascade_with_ctas(out, q, k_pool, v_pool, block_tables, context_le
     else:
         rc = lib.pa_decode_cascade_with_ctas(*args, int(num_ctas), *tail)
     _check(_name, rc)
+    return out
+
+
+def pa_decode_cascade_nested_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                           head_dim: int, max_blocks_per_seq: int,
+                                           num_ctas: int = 0) -> int:
+    return int(load().pa_decode_cascade_nested_workspace_size(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_ctas))
+
+
+def pa_decode_cascade_nested(out, q, k_pool, v_pool, block_tables, context_lens, cu_groups,
+                             prefix_lens, cu_siblings, sibling_lens, scale: float,
+                             num_ctas: int = 0, workspace=None, d_status=None, stream=None):
+    """Two-level cascade decode (see include/pa.h): groups sharing a prefix
+    (cu_groups / prefix_lens, may be empty) and sibling groups sharing a longer
+    one (cu_siblings / sibling_lens), each sibling entry's shared blocks read
+    once. q/out [S, Hq, d]. Returns out."""
+    lib = load()
+    pool = make_pool(k_pool, v_pool)
+    S, hq, d = q.shape
+    for name, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                    ("cu_groups", cu_groups), ("prefix_lens", prefix_lens),
+                    ("cu_siblings", cu_siblings), ("sibling_lens", sibling_lens)):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    ng = int(prefix_lens.shape[0])
+    nsib = int(sibling_lens.shape[0])
+    if int(cu_groups.shape[0]) != ng + 1:
+        raise ValueError("cu_groups must hold num_groups + 1 entries")
+    if int(cu_siblings.shape[0]) != nsib + 1:
+        raise ValueError("cu_siblings must hold num_sibling_groups + 1 entries")
+    mb = int(block_tables.shape[1])
+    hkv = int(k_pool.shape[2])
+    ws = _workspace(pa_decode_cascade_nested_workspace_size(S, hq, hkv, d, mb, int(num_ctas)),
+                    q.device, workspace)
+    rc = lib.pa_decode_cascade_nested(
+        ctypes.byref(pool), _ptr(out), _ptr(q), S, hq, _ptr(block_tables), mb,
+        _ptr(context_lens), _ptr(cu_groups), _ptr(prefix_lens), ng, _ptr(cu_siblings),
+        _ptr(sibling_lens), nsib, float(scale), int(num_ctas), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream))
+    _check("pa_decode_cascade_nested", rc)
     return out
 
 

@@ -192,14 +192,31 @@ int pa_decode(const pa_kv_pool* pool, void* out, const void* q, int num_seqs, in
 }
 
 namespace {
-// Cascade workspace: the decode workspace, then the prefix partials
-// (max, sum) [num_seqs, hq] float2 and accumulators [num_seqs, hq, head_dim] fp32.
-size_t cascade_ml_offset(int num_seqs, int num_q_heads, int head_dim) {
-  return align_up_sz(decode_workspace_bytes(num_seqs, num_q_heads, head_dim), 256);
+// Cascade workspace: the decode workspace (`slots` partial slots), then the
+// prefix partials (max, sum) [num_seqs, hq] float2 and accumulators
+// [num_seqs, hq, head_dim] fp32.
+size_t cascade_ml_offset(int num_seqs, int num_q_heads, int head_dim, size_t slots) {
+  return align_up_sz(decode_workspace_bytes_slots(num_seqs, num_q_heads, head_dim, slots), 256);
 }
-size_t cascade_acc_offset(int num_seqs, int num_q_heads, int head_dim) {
-  return cascade_ml_offset(num_seqs, num_q_heads, head_dim) +
+size_t cascade_acc_offset(int num_seqs, int num_q_heads, int head_dim, size_t slots) {
+  return cascade_ml_offset(num_seqs, num_q_heads, head_dim, slots) +
          align_up_sz(static_cast<size_t>(num_seqs) * num_q_heads * 8, 256);
+}
+// ... then the decode kernel's per-sequence records for the merge, [num_seqs] uint32
+size_t cascade_rec_offset(int num_seqs, int num_q_heads, int head_dim, size_t slots) {
+  return cascade_acc_offset(num_seqs, num_q_heads, head_dim, slots) +
+         align_up_sz(static_cast<size_t>(num_seqs) * num_q_heads * head_dim * 4, 256);
+}
+size_t cascade_bytes(int num_seqs, int num_q_heads, int head_dim, size_t slots) {
+  return cascade_rec_offset(num_seqs, num_q_heads, head_dim, slots) +
+         static_cast<size_t>(num_seqs) * 4;
+}
+size_t plain_slots(int num_seqs) { return static_cast<size_t>(kMaxDecodeCtas) + num_seqs; }
+// Sibling entries of up to 16 / G members: a member of an entry that spans n
+// CTAs leaves n partials, so the slots grow to num_seqs + (16 / G) * CTAs.
+size_t nested_slots(int num_seqs, int group, int num_ctas) {
+  const int ctas = num_ctas > 0 ? std::min(num_ctas, kMaxDecodeCtas) : kMaxDecodeCtas;
+  return static_cast<size_t>(num_seqs) + static_cast<size_t>(16 / group) * ctas;
 }
 
 // Decode beside prefill: the decode kernel (HBM-bound) runs on a reduced set
@@ -230,21 +247,33 @@ constexpr int kMixedTokensPerSeq = 12;
 size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int head_dim,
                                         int max_blocks_per_seq) {
   if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0) return 0;
-  return cascade_acc_offset(num_seqs, num_q_heads, head_dim) +
-         static_cast<size_t>(num_seqs) * num_q_heads * head_dim * 4;
+  return cascade_bytes(num_seqs, num_q_heads, head_dim, plain_slots(num_seqs));
 }
 
-int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
-                                int num_q_heads, const int32_t* block_tables,
-                                int max_blocks_per_seq, const int32_t* context_lens,
-                                const int32_t* cu_groups, const int32_t* prefix_lens,
-                                int num_groups, float scale, int num_ctas, void* workspace,
-                                size_t workspace_bytes, int* d_status, void* stream) {
-  pa::TraceRange trace("pa_decode_cascade");
+size_t pa_decode_cascade_nested_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                               int head_dim, int max_blocks_per_seq, int num_ctas) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_blocks_per_seq <= 0 || num_ctas < 0 || num_q_heads % num_kv_heads != 0)
+    return 0;
+  const int group = num_q_heads / num_kv_heads;
+  if (group > 16) return 0;
+  return cascade_bytes(num_seqs, num_q_heads, head_dim, nested_slots(num_seqs, group, num_ctas));
+}
+
+namespace {
+// Both cascade entry points: the first level (cu_groups / prefix_lens, the
+// tensor-core prefix pass) and, for the nested call, the second (cu_sib /
+// shared_lens, sibling entries in the decode kernel).
+int cascade_impl(const pa_kv_pool* pool, void* out, const void* q, int num_seqs, int num_q_heads,
+                 const int32_t* block_tables, int max_blocks_per_seq,
+                 const int32_t* context_lens, const int32_t* cu_groups,
+                 const int32_t* prefix_lens, int num_groups, const int32_t* cu_sib,
+                 const int32_t* shared_lens, int num_sib, bool nested, float scale, int num_ctas,
+                 void* workspace, size_t workspace_bytes, int* d_status, void* stream) {
   if (num_ctas < 0) return PA_EINVAL;
   int rc = check_pool(pool);
   if (rc != PA_OK) return rc;
-  if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_groups < 0) return PA_EINVAL;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_groups < 0 || num_sib < 0) return PA_EINVAL;
   rc = check_heads(pool, num_q_heads);
   if (rc != PA_OK) return rc;
   const int group = num_q_heads / pool->num_kv_heads;
@@ -255,14 +284,15 @@ int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q
   if (out == nullptr || q == nullptr || block_tables == nullptr || context_lens == nullptr)
     return PA_EINVAL;
   if (num_groups > 0 && (cu_groups == nullptr || prefix_lens == nullptr)) return PA_EINVAL;
+  if (num_sib > 0 && (cu_sib == nullptr || shared_lens == nullptr)) return PA_EINVAL;
   if (!aligned16(out) || !aligned16(q)) return PA_EINVAL;
-  const size_t need = pa_decode_cascade_workspace_size(num_seqs, num_q_heads, pool->head_dim,
-                                                       max_blocks_per_seq);
+  const size_t slots = nested ? nested_slots(num_seqs, group, num_ctas) : plain_slots(num_seqs);
+  const size_t need = cascade_bytes(num_seqs, num_q_heads, pool->head_dim, slots);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PA_EWORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  void* pre_ml = ws + cascade_ml_offset(num_seqs, num_q_heads, pool->head_dim);
-  void* pre_acc = ws + cascade_acc_offset(num_seqs, num_q_heads, pool->head_dim);
+  void* pre_ml = ws + cascade_ml_offset(num_seqs, num_q_heads, pool->head_dim, slots);
+  void* pre_acc = ws + cascade_acc_offset(num_seqs, num_q_heads, pool->head_dim, slots);
   DecodeArgs a = {};
   a.pool = view(pool);
   a.out = out;
@@ -279,6 +309,13 @@ int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q
   a.workspace_bytes = workspace_bytes;
   a.d_status = d_status;
   a.grid_override = num_ctas;
+  a.ws_slots = slots;
+  a.ws_rec = ws + cascade_rec_offset(num_seqs, num_q_heads, pool->head_dim, slots);
+  if (num_sib > 0) {
+    a.cu_sib = cu_sib;
+    a.shared_lens = shared_lens;
+    a.num_sib = num_sib;
+  }
   if (num_groups == 0) return to_status(launch_decode(a, st));
   a.cu_groups = cu_groups;
   a.prefix_lens = prefix_lens;
@@ -314,6 +351,33 @@ int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q
   if (rc != PA_OK) return rc;
   a.launch_part = 2;
   return to_status(launch_decode(a, st));
+}
+}  // namespace
+
+int pa_decode_cascade_with_ctas(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+                                int num_q_heads, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens,
+                                const int32_t* cu_groups, const int32_t* prefix_lens,
+                                int num_groups, float scale, int num_ctas, void* workspace,
+                                size_t workspace_bytes, int* d_status, void* stream) {
+  pa::TraceRange trace("pa_decode_cascade");
+  return cascade_impl(pool, out, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                      context_lens, cu_groups, prefix_lens, num_groups, nullptr, nullptr, 0, false,
+                      scale, num_ctas, workspace, workspace_bytes, d_status, stream);
+}
+
+int pa_decode_cascade_nested(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,
+                             int num_q_heads, const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, const int32_t* cu_groups,
+                             const int32_t* prefix_lens, int num_groups,
+                             const int32_t* cu_siblings, const int32_t* sibling_lens,
+                             int num_sibling_groups, float scale, int num_ctas, void* workspace,
+                             size_t workspace_bytes, int* d_status, void* stream) {
+  pa::TraceRange trace("pa_decode_cascade_nested");
+  return cascade_impl(pool, out, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                      context_lens, cu_groups, prefix_lens, num_groups, cu_siblings, sibling_lens,
+                      num_sibling_groups, true, scale, num_ctas, workspace, workspace_bytes,
+                      d_status, stream);
 }
 
 int pa_decode_cascade(const pa_kv_pool* pool, void* out, const void* q, int num_seqs,

@@ -5,10 +5,15 @@
 namespace pa {
 
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim) {
+  return decode_workspace_bytes_slots(num_seqs, num_q_heads, head_dim,
+                                      static_cast<size_t>(kMaxDecodeCtas) + num_seqs);
+}
+
+size_t decode_workspace_bytes_slots(int num_seqs, int num_q_heads, int head_dim, size_t slots) {
   // [num_seqs + 1] block prefix, then per partial slot (CTA c, sequence s at
-  // slot c + s) the (max, sum) pair and the fp32 accumulator of every head
+  // slot c + s without sibling groups) the (max, sum) pair and the fp32
+  // accumulator of every head
   const size_t prefix_bytes = align_up_sz((num_seqs + 1) * 4, 256);
-  const size_t slots = static_cast<size_t>(kMaxDecodeCtas) + num_seqs;
   const size_t ml = align_up_sz(slots * num_q_heads * 8, 256);
   const size_t acc = slots * num_q_heads * static_cast<size_t>(head_dim) * 4;
   return prefix_bytes + ml + acc;

@@ -67,6 +67,11 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTableCache = 1024;     // block-table entries staged in shared memory
 constexpr float kRescaleThreshold = 8.0f;
+// Initial running max of a tensor-core row: finite, so that a row masked for
+// a whole block (another member's block) gets weights 2^(-inf - m) = 0, and
+// far enough below any score that the first real one replaces it (the
+// rescale factor 2^(kNoMax - m) is 0).
+constexpr float kNoMax = -1e30f;
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -157,13 +162,16 @@ struct SmemLayout {
   int tokens_per_unit;  // tokens of one block moved per pipeline stage (16, 8 or 4)
   int parts;            // 16 / tokens_per_unit
   int part_bytes;       // one K (or V) part: tokens_per_unit * Hkv * D * elt
-  int off_bars, off_done, off_flags, off_mbars, off_table, off_ntok, off_merge, off_prefix, total;
+  int off_bars, off_done, off_flags, off_mbars, off_table, off_ntok, off_memb, off_merge, off_prefix,
+      off_meta;  // staged cascade metadata (0: not staged)
+  int total;
 };
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline SmemLayout make_layout(int stages, int tokens_per_unit, int hkv, int d,
-                                                  int elt, int wh, int group, int num_seqs) {
+                                                  int elt, int wh, int group, int num_seqs,
+                                                  int meta_ints) {
   SmemLayout L;
   L.stages = stages;
   L.tokens_per_unit = tokens_per_unit;
@@ -172,14 +180,17 @@ __host__ __device__ inline SmemLayout make_layout(int stages, int tokens_per_uni
   const int off = stages * 2 * L.part_bytes;
   L.off_bars = align_up(off, 16);
   L.off_done = L.off_bars + stages * 8;
-  L.off_flags = L.off_done + stages * 4;
-  L.off_mbars = align_up(L.off_flags + stages * 4, 16);   // 2 merge mbarriers per KV head
+  L.off_flags = L.off_done + stages * 4;  // [stages] valid tokens, then [stages] member masks
+  L.off_mbars = align_up(L.off_flags + stages * 8, 16);   // 2 merge mbarriers per KV head
   L.off_table = align_up(L.off_mbars + 2 * hkv * 8, 16);
   L.off_ntok = L.off_table + kTableCache * 4;  // valid tokens of each cached block
-  L.off_merge = align_up(L.off_ntok + kTableCache, 16);
+  L.off_memb = L.off_ntok + kTableCache;       // member mask of each cached block (uint16)
+  L.off_merge = align_up(L.off_memb + 2 * kTableCache, 16);
   const int merge_bytes = (wh - 1) * hkv * group * (d + 2) * 4;
   L.off_prefix = align_up(L.off_merge + merge_bytes, 16);
-  L.total = align_up(L.off_prefix + (num_seqs + 1) * 4, 128) + 1024;  // + base alignment
+  const int end = align_up(L.off_prefix + (num_seqs + 1) * 4, 16);
+  L.off_meta = meta_ints > 0 ? end : 0;
+  L.total = align_up(end + meta_ints * 4, 128) + 1024;  // + base alignment
   return L;
 }
 
@@ -213,15 +224,43 @@ struct DecodeParams {
   // decode kernel leaves every cascade sequence as a partial and only the
   // merge kernel, ordered after both, folds the prefix in
   int defer_prefix;
+  // nested cascade, second level (tensor-core path only; cu_sib == nullptr
+  // otherwise): sequences cu_sib[j] .. cu_sib[j+1]-1 share their first
+  // shared_lens[j] tokens (whole blocks, at least the first level's prefix).
+  // They are walked in entries of up to sib_m consecutive members whose query
+  // rows fill one 16-row MMA tile, so a shared block is read once per entry.
+  const int32_t* cu_sib;
+  const int32_t* shared_lens;
+  int num_sib;
+  int sib_m;  // members per entry: 16 / G with sibling groups, else 1
+  int64_t num_slots;  // partial slots in the workspace
+  // cascade calls: per sequence, written by CTA 0 for the merge kernel: bits
+  // 0-3 its offset in its entry, 4-8 the entry's member count, 9 valid
+  // lengths, 10 a first-level prefix partial
+  uint32_t* ws_rec;
   // tensor-core path: the K and V pools as 4-D maps (see make_tmap_pool_heads)
   CUtensorMap tm_k;
   CUtensorMap tm_v;
 };
 
+// The per-sequence inputs the block walk reads (same names as in
+// DecodeParams): a cascade call stages them in shared memory, so that the
+// prologue's scan and the lookups of every block and entry search on chip.
+struct SeqMeta {
+  const int32_t* context_lens;
+  const int32_t* cu_q_lens;
+  const int32_t* cu_groups;
+  const int32_t* prefix_lens;
+  const int32_t* cu_sib;
+  const int32_t* shared_lens;
+  int num_seqs, num_rows, max_blocks, num_groups, num_sib, sib_m;
+};
+
 // Leading blocks of sequence s whose attention is already in its group's
 // shared-prefix partial (0 without groups or outside every group). A prefix
 // that is not whole blocks, or longer than the context, is flagged.
-__device__ __forceinline__ int prefix_blocks(const DecodeParams& p, int s, int ctx, bool* bad) {
+template <class P>
+__device__ __forceinline__ int prefix_blocks(const P& p, int s, int ctx, bool* bad) {
   if (p.cu_groups == nullptr || p.num_groups <= 0) return 0;
   if (s < p.cu_groups[0] || s >= p.cu_groups[p.num_groups]) return 0;
   const int g = upper_index(p.cu_groups, p.num_groups, s);
@@ -234,9 +273,52 @@ __device__ __forceinline__ int prefix_blocks(const DecodeParams& p, int s, int c
   return len / kBlockSize;
 }
 
+// Sibling group of sequence s (second cascade level), or -1. A group whose
+// bounds leave [0, num_seqs] is ignored (its members are walked alone), so
+// no entry reaches past the batch.
+template <class P>
+__device__ __forceinline__ int sib_group(const P& p, int s) {
+  if (p.cu_sib == nullptr || p.num_sib <= 0) return -1;
+  if (s < p.cu_sib[0] || s >= p.cu_sib[p.num_sib]) return -1;
+  const int j = upper_index(p.cu_sib, p.num_sib, s);
+  const int g0 = p.cu_sib[j], g1 = p.cu_sib[j + 1];
+  return g0 >= 0 && s >= g0 && s < g1 && g1 <= p.num_seqs ? j : -1;
+}
+
+// First member of the entry holding sequence s of sibling group j: members
+// are taken sib_m at a time from the group's first sequence.
+template <class P>
+__device__ __forceinline__ int entry_start(const P& p, int j, int s) {
+  const int g0 = p.cu_sib[j];
+  return g0 + (s - g0) / p.sib_m * p.sib_m;
+}
+
+// The entry (first member a, k members) of sequence s; (s, 1) outside every
+// sibling group.
+template <class P>
+__device__ __forceinline__ void entry_of(const P& p, int s, int* a, int* k) {
+  const int j = sib_group(p, s);
+  if (j < 0) {
+    *a = s;
+    *k = 1;
+    return;
+  }
+  *a = entry_start(p, j, s);
+  *k = min(p.sib_m, p.cu_sib[j + 1] - *a);
+}
+
+// The CTA whose range holds block b of the decode order (B blocks, `grid`
+// CTAs; CTA c holds blocks [c B / grid, (c + 1) B / grid)).
+__host__ __device__ __forceinline__ int64_t cta_of_block(int64_t b, int64_t B, int64_t grid) {
+  return ((b + 1) * grid - 1) / B;
+}
+
 // Blocks the decode kernel reads for sequence s (0 when s is not a decode
-// sequence or its lengths are invalid).
-__device__ __forceinline__ int decode_blocks(const DecodeParams& p, int s, bool* bad) {
+// sequence or its lengths are invalid). A sibling group's shared blocks after
+// the first-level prefix are counted once per entry, as blocks of its first
+// member; the other members count only their own blocks.
+template <class P>
+__device__ __forceinline__ int decode_blocks(const P& p, int s, bool* bad) {
   int q_len = 1;
   if (p.cu_q_lens != nullptr) {
     q_len = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
@@ -257,7 +339,56 @@ __device__ __forceinline__ int decode_blocks(const DecodeParams& p, int s, bool*
     *bad = true;
     return 0;
   }
-  return (ctx + kBlockSize - 1) / kBlockSize - skip;
+  const int j = sib_group(p, s);
+  if (j < 0) return (ctx + kBlockSize - 1) / kBlockSize - skip;
+  // the shared blocks are read through the entry's first member's table: its
+  // lengths must hold them too, with the same first-level prefix
+  const int shared = p.shared_lens[j];
+  if (shared < skip * kBlockSize || shared % kBlockSize != 0 || shared > ctx) {
+    *bad = true;
+    return 0;
+  }
+  const int a = entry_start(p, j, s);
+  if (a != s) {
+    const int ctx_a = p.context_lens[a];
+    bool bad_a = false;
+    if (ctx_a < 1 || ctx_a > p.max_blocks * kBlockSize || shared > ctx_a ||
+        prefix_blocks(p, a, ctx_a, &bad_a) != skip || bad_a) {
+      *bad = true;
+      return 0;
+    }
+  }
+  const int own = (ctx + kBlockSize - 1) / kBlockSize - shared / kBlockSize;
+  return own + (a == s ? shared / kBlockSize - skip : 0);
+}
+
+// Where sequence s's blocks start in its block table (logical block `first`)
+// and which rows of its entry attend them: blocks before `shared_end` are the
+// sibling group's shared blocks (every member's rows), the rest are s's own.
+struct SeqWalk {
+  int first;
+  int shared_end;
+  uint32_t shared_mask;
+  uint32_t own_mask;
+};
+template <class P>
+__device__ __forceinline__ SeqWalk seq_walk(const P& p, int s, int ctx) {
+  bool unused = false;
+  SeqWalk w;
+  w.first = prefix_blocks(p, s, ctx, &unused);
+  w.shared_end = 0;
+  w.shared_mask = 1u;
+  w.own_mask = 1u;
+  const int j = sib_group(p, s);
+  if (j >= 0) {
+    const int a = entry_start(p, j, s);
+    const int k = min(p.sib_m, p.cu_sib[j + 1] - a);
+    w.shared_end = p.shared_lens[j] / kBlockSize;
+    w.own_mask = 1u << (s - a);
+    if (a == s) w.shared_mask = (1u << k) - 1u;
+    else w.first = w.shared_end;
+  }
+  return w;
 }
 
 __device__ __forceinline__ int query_row(const DecodeParams& p, int s) {
@@ -300,10 +431,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
   int* done = reinterpret_cast<int*>(smem + L.off_done);
   int* flags = reinterpret_cast<int*>(smem + L.off_flags);
+  uint32_t* memb = reinterpret_cast<uint32_t*>(flags + L.stages);  // rows of the entry per stage
   uint64_t* merge_full = reinterpret_cast<uint64_t*>(smem + L.off_mbars);
   uint64_t* merge_empty = merge_full + HKV;
   int* table = reinterpret_cast<int*>(smem + L.off_table);
   uint8_t* block_ntok = reinterpret_cast<uint8_t*>(smem + L.off_ntok);
+  uint16_t* block_memb = reinterpret_cast<uint16_t*>(smem + L.off_memb);
   float* merge = reinterpret_cast<float*>(smem + L.off_merge);
   int* prefix = reinterpret_cast<int*>(smem + L.off_prefix);
   __shared__ int warp_sums[kWarps];
@@ -323,16 +456,71 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     fence_mbar_init();
   }
+  // the block walk's per-sequence inputs: staged in shared memory for a
+  // cascade call (context lengths, group and sibling bounds and lengths)
+  __shared__ SeqMeta meta;
+  if (L.off_meta > 0) {
+    int32_t* m_ctx = reinterpret_cast<int32_t*>(smem + L.off_meta);
+    int32_t* m_cu = m_ctx + S;
+    int32_t* m_pl = m_cu + (p.num_groups > 0 ? p.num_groups + 1 : 0);
+    int32_t* m_sib = m_pl + (p.num_groups > 0 ? p.num_groups : 0);
+    int32_t* m_sl = m_sib + (p.num_sib > 0 ? p.num_sib + 1 : 0);
+    for (int i = tid; i < S; i += kThreads) m_ctx[i] = p.context_lens[i];
+    if (p.num_groups > 0) {
+      for (int i = tid; i <= p.num_groups; i += kThreads) m_cu[i] = p.cu_groups[i];
+      for (int i = tid; i < p.num_groups; i += kThreads) m_pl[i] = p.prefix_lens[i];
+    }
+    if (p.num_sib > 0) {
+      for (int i = tid; i <= p.num_sib; i += kThreads) m_sib[i] = p.cu_sib[i];
+      for (int i = tid; i < p.num_sib; i += kThreads) m_sl[i] = p.shared_lens[i];
+    }
+    if (tid == 0) {
+      meta.context_lens = m_ctx;
+      meta.cu_groups = p.num_groups > 0 ? m_cu : p.cu_groups;
+      meta.prefix_lens = p.num_groups > 0 ? m_pl : p.prefix_lens;
+      meta.cu_sib = p.num_sib > 0 ? m_sib : p.cu_sib;
+      meta.shared_lens = p.num_sib > 0 ? m_sl : p.shared_lens;
+    }
+  } else if (tid == 0) {
+    meta.context_lens = p.context_lens;
+    meta.cu_groups = p.cu_groups;
+    meta.prefix_lens = p.prefix_lens;
+    meta.cu_sib = p.cu_sib;
+    meta.shared_lens = p.shared_lens;
+  }
+  if (tid == 0) {
+    meta.cu_q_lens = p.cu_q_lens;
+    meta.num_seqs = S;
+    meta.num_rows = p.num_rows;
+    meta.max_blocks = p.max_blocks;
+    meta.num_groups = p.num_groups;
+    meta.num_sib = p.num_sib;
+    meta.sib_m = p.sib_m;
+  }
+  __syncthreads();
   bool bad_len = false;
   block_exclusive_scan<kThreads>(
-      S, [&](int s) { return decode_blocks(p, s, &bad_len); }, prefix, warp_sums);
+      S, [&](int s) { return decode_blocks(meta, s, &bad_len); }, prefix, warp_sums);
   if (bad_len && blockIdx.x == 0) status_or(p.d_status, PA_STATUS_BAD_LENGTH);
+
+  // cascade calls: the merge kernel's per-sequence record (see DecodeParams)
+  if (blockIdx.x == 0 && p.ws_rec != nullptr) {
+    for (int s = tid; s < S; s += kThreads) {
+      int a = s, k = 1;
+      entry_of(meta, s, &a, &k);
+      bool bad = false, pre_bad = false;
+      decode_blocks(meta, s, &bad);
+      const bool hp = prefix_blocks(meta, s, meta.context_lens[s], &pre_bad) > 0;
+      p.ws_rec[s] = static_cast<uint32_t>(s - a) | (static_cast<uint32_t>(k) << 4) |
+                    (bad ? 0u : 1u << 9) | (hp ? 1u << 10 : 0u);
+    }
+  }
 
   // Invalid decode sequences (bad lengths) get zero output rows, written once:
   // one warp of the grid checks each sequence, so no CTA lags the others
   for (int s = blockIdx.x * kWarps + warp; s < S; s += gridDim.x * kWarps) {
     bool bad = false;
-    const bool decode_row = decode_blocks(p, s, &bad) > 0 || bad;
+    const bool decode_row = decode_blocks(meta, s, &bad) > 0 || bad;
     int q_len = 1;
     if (p.cu_q_lens != nullptr) q_len = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
     const int row = query_row(p, s);
@@ -362,17 +550,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int rel = parts == 1 ? u : u / parts;  // block of the CTA's range
     const int part = parts == 1 ? 0 : u % parts;
     int phys, block_tokens;
+    uint32_t rows;
     if (rel < kTableCache && !direct) {
       phys = table[rel];
       block_tokens = block_ntok[rel];
+      rows = block_memb[rel];
     } else {
       const int s = upper_index(prefix, S, lo + rel);
-      bool unused = false;
-      const int j = static_cast<int>(lo + rel - prefix[s]) +  // logical block of sequence s
-                    prefix_blocks(p, s, p.context_lens[s], &unused);
+      const int ctx = meta.context_lens[s];
+      const SeqWalk sw = seq_walk(meta, s, ctx);
+      const int j = static_cast<int>(lo + rel - prefix[s]) + sw.first;  // logical block of s
       phys = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
-      block_tokens = min(kBlockSize, p.context_lens[s] - j * kBlockSize);
+      block_tokens = min(kBlockSize, ctx - j * kBlockSize);
+      rows = j < sw.shared_end ? sw.shared_mask : sw.own_mask;
     }
+    memb[st] = rows;
     const int ntok = min(tpu, block_tokens - part * tpu);
     if (phys < 0 || phys >= p.num_blocks) {
       flags[st] = -1;
@@ -414,10 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const int n_cached = static_cast<int>(min(hi - lo, static_cast<int64_t>(kTableCache)));
   for (int i = tid; i < n_cached; i += kThreads) {
     const int s = upper_index(prefix, S, lo + i);
-    bool unused = false;
-    const int j = static_cast<int>(lo + i - prefix[s]) + prefix_blocks(p, s, p.context_lens[s], &unused);
+    const int ctx = meta.context_lens[s];
+    const SeqWalk sw = seq_walk(meta, s, ctx);
+    const int j = static_cast<int>(lo + i - prefix[s]) + sw.first;
     table[i] = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
-    block_ntok[i] = static_cast<uint8_t>(min(kBlockSize, p.context_lens[s] - j * kBlockSize));
+    block_ntok[i] = static_cast<uint8_t>(min(kBlockSize, ctx - j * kBlockSize));
+    block_memb[i] = static_cast<uint16_t>(j < sw.shared_end ? sw.shared_mask : sw.own_mask);
   }
   __syncthreads();
   // the merge kernel may be launched now: it waits (griddepcontrol.wait) for
@@ -452,42 +646,67 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     int u = 0;
     int st_c = 0;
     uint32_t ph_c = 0;
+    // tile rows gi and gi + 8 of this lane: query head (row % G) of member
+    // (row / G) of the current entry
+    const int mr0 = gi / G, mr1 = (gi + 8) / G;
     int s = upper_index(prefix, S, lo);
     bool ok = true;
     while (u < n_units && ok) {
       while (prefix[s + 1] <= lo + (parts == 1 ? u : u / parts)) ++s;
-      const int64_t seq_lo = max(lo, static_cast<int64_t>(prefix[s]));
-      const int64_t seq_hi = min(hi, static_cast<int64_t>(prefix[s + 1]));
-      const int64_t seq_units = (seq_hi - seq_lo) * parts;
-      const bool whole = prefix[s] >= lo && prefix[s + 1] <= hi;
-      const int row = query_row(p, s);
-      bool pre_bad = false;
-      const bool has_pre = prefix_blocks(p, s, p.context_lens[s], &pre_bad) > 0;
+      // the entry holding s: members a .. a + k - 1, blocks [e_lo, e_hi)
+      int a = s, k = 1;
+      if (p.cu_sib != nullptr) entry_of(meta, s, &a, &k);
+      const int64_t e_lo = prefix[a], e_hi = prefix[a + k];
+      // units from here to the end of the entry or of the range (counted from
+      // the current unit, so that even inconsistent sibling bounds cannot
+      // make the walk repeat or overrun units)
+      const int64_t seq_units = (min(hi, e_hi) - lo) * parts - u;
+      const bool whole = e_lo >= lo && e_hi <= hi;
+      // members with valid lengths (a member with bad ones may sit in an
+      // entry whose shared blocks are read; its row stays zero) and members
+      // with a first-level prefix partial, one lane per member
+      uint32_t vmask, pmask;
+      {
+        bool v = false, hp = false;
+        if (lane < k) {
+          const int sq = a + lane;
+          bool bad = false;
+          if (k > 1) decode_blocks(meta, sq, &bad);
+          v = !bad;
+          bool pre_bad = false;
+          hp = prefix_blocks(meta, sq, meta.context_lens[sq], &pre_bad) > 0;
+        }
+        vmask = __ballot_sync(0xffffffffu, v);
+        pmask = __ballot_sync(0xffffffffu, hp);
+      }
       // Q as stored (bf16 pairs); the scale is applied to the fp32 scores
       {
-        const uint32_t* q = reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) +
-                                                              static_cast<int64_t>(row) * p.hq * D);
-        const int h0 = g * G + gi, h1 = g * G + gi + 8;
+        const bool in0 = mr0 < k, in1 = mr1 < k;
+        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
+            static_cast<const T*>(p.q) + static_cast<int64_t>(query_row(p, a + (in0 ? mr0 : 0))) * p.hq * D);
+        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
+            static_cast<const T*>(p.q) + static_cast<int64_t>(query_row(p, a + (in1 ? mr1 : 0))) * p.hq * D);
+        const int h0 = g * G + gi % G, h1 = g * G + (gi + 8) % G;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           const int c = (16 * kk + 2 * qi) / 2;  // bf16-pair index
-          qa[kk][0] = gi < G ? __ldg(q + h0 * (D / 2) + c) : 0u;
-          qa[kk][1] = gi + 8 < G ? __ldg(q + h1 * (D / 2) + c) : 0u;
-          qa[kk][2] = gi < G ? __ldg(q + h0 * (D / 2) + c + 4) : 0u;
-          qa[kk][3] = gi + 8 < G ? __ldg(q + h1 * (D / 2) + c + 4) : 0u;
+          qa[kk][0] = in0 ? __ldg(q0 + h0 * (D / 2) + c) : 0u;
+          qa[kk][1] = in1 ? __ldg(q1 + h1 * (D / 2) + c) : 0u;
+          qa[kk][2] = in0 ? __ldg(q0 + h0 * (D / 2) + c + 4) : 0u;
+          qa[kk][3] = in1 ? __ldg(q1 + h1 * (D / 2) + c + 4) : 0u;
         }
       }
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-      bool poisoned = false;
+      float m0 = kNoMax, m1 = kNoMax, l0 = 0.f, l1 = 0.f;
+      uint32_t poison = 0;  // members whose rows met a bad block
 
       for (int su = 0; su < seq_units; ++su, ++u) {
         const int st = st_c;
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], ph_c));
         if (!ok) break;
         const int ntok = flags[st];
-        if (ntok < 0) poisoned = true;
+        if (ntok < 0) poison |= memb[st];
         if (ntok > 0) {
           const uint32_t kb = sbase + static_cast<uint32_t>(st * 2 * L.part_bytes);
           const uint32_t vb = kb + static_cast<uint32_t>(L.part_bytes);
@@ -515,15 +734,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             mma_16816(sc[0], qa[kk], kf[0], kf[1]);
             mma_16816(sc[1], qa[kk], kf[2], kf[3]);
           }
-          // log2-domain scores; tokens past the context are masked
+          // log2-domain scores; tokens past the context, and every token for
+          // rows of members that do not attend this block (another member's
+          // own block), are masked
+          const uint32_t rows = memb[st];
+          const int nt0 = (rows >> mr0) & 1u ? ntok : 0, nt1 = (rows >> mr1) & 1u ? ntok : 0;
           float mt0 = -INFINITY, mt1 = -INFINITY;
 #pragma unroll
           for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const bool valid = 8 * n + 2 * qi + e < ntok;  // token of column 2qi+e of n-tile n
-              sc[n][e] = valid ? sc[n][e] * p.scale_log2 : -INFINITY;
-              sc[n][2 + e] = valid ? sc[n][2 + e] * p.scale_log2 : -INFINITY;
+              const int col = 8 * n + 2 * qi + e;  // token of column 2qi+e of n-tile n
+              sc[n][e] = col < nt0 ? sc[n][e] * p.scale_log2 : -INFINITY;
+              sc[n][2 + e] = col < nt1 ? sc[n][2 + e] * p.scale_log2 : -INFINITY;
               mt0 = fmaxf(mt0, sc[n][e]);
               mt1 = fmaxf(mt1, sc[n][2 + e]);
             }
@@ -536,8 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           const bool need0 = mt0 > m0 + kRescaleThreshold, need1 = mt1 > m1 + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need0 || need1)) {
             const float n0 = need0 ? mt0 : m0, n1 = need1 ? mt1 : m1;
-            const float a0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - n0);
-            const float a1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - n1);
+            const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);  // 0 from kNoMax
             l0 *= a0;
             l1 *= a1;
 #pragma unroll
@@ -595,28 +817,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
       }
+      // partial slots of the entry: member m in CTA c (c_f <= c < c_f + n_c)
+      // writes slot a + c_f sib_m + m n_c + (c - c_f), unique over the batch
+      // since entries and CTA ranges are both in block order (c + s without
+      // sibling groups)
+      const int64_t c_f = cta_of_block(e_lo, prefix[S], gridDim.x);
+      const int64_t n_c = cta_of_block(e_hi - 1, prefix[S], gridDim.x) - c_f + 1;
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const int hr = gi + 8 * r;  // row of the tile = query head of the group
-        if (hr >= G) continue;
-        const int head = g * G + hr;
-        float mr = r ? m1 : m0, lr_ = r ? l1 : l0;
+        const int mr = r ? mr1 : mr0;  // member of the entry
+        if (mr >= k || !((vmask >> mr) & 1u)) continue;
+        const int sq = a + mr;
+        const int row = query_row(p, sq);
+        const bool has_pre = (pmask >> mr) & 1u;
+        const bool poisoned = (poison >> mr) & 1u;
+        const int head = g * G + (gi + 8 * r) % G;
+        const float mx = r ? m1 : m0;
+        float lr_ = r ? l1 : l0;
         if (whole && !(has_pre && p.defer_prefix)) {
           bool pre_poisoned = false;
           if (has_pre) {
             // fold in the shared-prefix partial of this sequence
-            const int64_t idx = static_cast<int64_t>(s) * p.hq + head;
+            const int64_t idx = static_cast<int64_t>(sq) * p.hq + head;
             const float2 pml = p.pre_ml[idx];
             pre_poisoned = pml.y < 0.f;
-            const float mn = fmaxf(mr, pml.x);
-            const float a = merge_factor(mr, mn), b = merge_factor(pml.x, mn);
-            lr_ = lr_ * a + pml.y * b;
+            const float mn = fmaxf(mx, pml.x);
+            const float fa = merge_factor(mx, mn), fb = merge_factor(pml.x, mn);
+            lr_ = lr_ * fa + pml.y * fb;
             const float* prow = p.pre_acc + idx * D;
 #pragma unroll
             for (int n = 0; n < D / 8; ++n) {
               const float2 pv = *reinterpret_cast<const float2*>(prow + 8 * n + 2 * qi);
-              o[n][2 * r] = o[n][2 * r] * a + pv.x * b;
-              o[n][2 * r + 1] = o[n][2 * r + 1] * a + pv.y * b;
+              o[n][2 * r] = o[n][2 * r] * fa + pv.x * fb;
+              o[n][2 * r + 1] = o[n][2 * r + 1] * fa + pv.y * fb;
             }
           }
           const float inv = (poisoned || pre_poisoned) ? 0.f : 1.f / lr_;
@@ -626,8 +859,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           for (int n = 0; n < D / 8; ++n)
             orow[4 * n + qi] = pack_bf16x2(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
         } else {
-          const int64_t slot = static_cast<int64_t>(blockIdx.x) + s;
-          if (qi == 0) p.ws_ml[slot * p.hq + head] = make_float2(mr, poisoned ? -1.f : lr_);
+          const int64_t slot = a + c_f * p.sib_m + mr * n_c + (static_cast<int64_t>(blockIdx.x) - c_f);
+          if (slot < 0 || slot >= p.num_slots) continue;  // only with inconsistent sibling bounds
+          if (qi == 0) p.ws_ml[slot * p.hq + head] = make_float2(mx, poisoned ? -1.f : lr_);
           float* arow = p.ws_acc + (slot * p.hq + head) * D;
 #pragma unroll
           for (int n = 0; n < D / 8; ++n)
@@ -670,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const bool whole = prefix[s] >= lo && prefix[s + 1] <= hi;
     const int row = query_row(p, s);
     bool pre_bad = false;
-    const bool has_pre = prefix_blocks(p, s, p.context_lens[s], &pre_bad) > 0;
+    const bool has_pre = prefix_blocks(meta, s, meta.context_lens[s], &pre_bad) > 0;
 
     // this lane's query heads, pre-scaled into the log2 domain
     {
@@ -1112,30 +1346,31 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
       pacc[e + 1] = x.y;
     }
   }
+  // the entry holding s (members ea .. ea + ek - 1; s alone without sibling
+  // groups) and whether s has a first-level prefix partial, from the decode
+  // kernel's per-sequence record in a cascade call
+  int ea = s, ek = 1;
+  bool has_pre = false;
+  if (p.ws_rec != nullptr) {
+    const uint32_t rec = p.ws_rec[s];
+    if (!((rec >> 9) & 1u)) return;  // bad lengths: zeroed by the decode kernel
+    ea = s - static_cast<int>(rec & 15u);
+    ek = static_cast<int>((rec >> 4) & 31u);
+    has_pre = (rec >> 10) & 1u;
+  }
   const int* prefix = p.ws_prefix;
   const int64_t B = prefix[p.num_seqs];
-  const int64_t a0 = prefix[s], a1 = prefix[s + 1];
+  const int64_t a0 = prefix[ea], a1 = prefix[ea + ek];
   // CTA c covers blocks [c*B/grid, (c+1)*B/grid)
   int64_t c_first = 0, c_last = -1;  // no CTA partials when the suffix is empty
   if (a1 > a0) {
-    c_first = ((a0 + 1) * grid - 1) / B;
-    c_last = (a1 * grid - 1) / B;
-    // one CTA saw the whole sequence: it wrote the final row, unless the
+    c_first = cta_of_block(a0, B, grid);
+    c_last = cta_of_block(a1 - 1, B, grid);
+    // one CTA saw the whole entry: it wrote the final row, unless the
     // prefix fold was left to this kernel
-    if (c_first == c_last && !p.defer_prefix) return;
-  } else if (p.cu_groups == nullptr) {
-    return;  // not a decode sequence, or zeroed by the decode kernel
-  }
-  bool has_pre = false;
-  if (p.cu_groups != nullptr) {
-    bool bad = false;
-    if (a1 <= a0) {
-      decode_blocks(p, s, &bad);
-      if (bad) return;  // zeroed by the decode kernel
-    }
-    has_pre = prefix_blocks(p, s, p.context_lens[s], &bad) > 0;
-    if (a1 <= a0 && !has_pre) return;
-    if (a1 > a0 && c_first == c_last && !has_pre) return;  // finished by the decode kernel
+    if (c_first == c_last && !(p.defer_prefix && has_pre)) return;
+  } else if (!has_pre) {
+    return;  // not a decode sequence, zeroed by the decode kernel, or nothing to merge
   }
   float m = -INFINITY, l = 0.f;
   float acc[kPer];
@@ -1144,6 +1379,9 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
   bool poisoned = false;
   // with at least as many blocks as CTAs no CTA range is empty: skip the test
   const bool all_nonempty = B >= grid;
+  // this member's partial of CTA c sits at slot0 + c (see the decode kernel)
+  const int64_t slot0 = ea + c_first * p.sib_m + static_cast<int64_t>(s - ea) * (c_last - c_first + 1) -
+                        c_first;
   for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
     float2 ml[4];
     float v[4][kPer];
@@ -1152,9 +1390,13 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
     for (int j = 0; j < 4; ++j) {
       const int64_t c = c0 + j;
       use[j] = c <= c_last && (all_nonempty || c * B / grid != (c + 1) * B / grid);
+      if (use[j] && (slot0 + c < 0 || slot0 + c >= p.num_slots)) {
+        use[j] = false;  // only with inconsistent sibling bounds
+        poisoned = true;
+      }
       if (use[j]) {
-        ml[j] = p.ws_ml[(c + s) * p.hq + h];
-        const float* src = p.ws_acc + ((c + s) * p.hq + h) * D + lane * kPer;
+        ml[j] = p.ws_ml[(slot0 + c) * p.hq + h];
+        const float* src = p.ws_acc + ((slot0 + c) * p.hq + h) * D + lane * kPer;
 #pragma unroll
         for (int e = 0; e < kPer; e += 2) {
           const float2 x = *reinterpret_cast<const float2*>(src + e);
@@ -1198,13 +1440,32 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   int tpu = kBlockSize;
   while (tpu > 4 && 2 * tpu * token_bytes > 64 * 1024) tpu /= 2;
   const int smem_limit = 227 * 1024 - 1024;  // leave room for static shared memory
-  SmemLayout L = make_layout(4, tpu, hkv, D, elt, WH, G, a.num_seqs);
-  if (L.total > smem_limit) L = make_layout(3, tpu, hkv, D, elt, WH, G, a.num_seqs);
-  if (L.total > smem_limit) L = make_layout(2, tpu, hkv, D, elt, WH, G, a.num_seqs);
+  // sibling entries need the tensor-core path (their members share one MMA
+  // tile); elsewhere every sequence is walked on its own, which gives the
+  // same attention
+  const bool sib = Cfg<T, D, G, WH>::kMma && a.cu_sib != nullptr && a.num_sib > 0;
+  // a cascade call stages its per-sequence inputs in shared memory when they
+  // fit beside the stages (they are read from global memory otherwise)
+  const bool cascade = a.cu_groups != nullptr || sib;
+  const int meta_ints = cascade ? a.num_seqs + (a.num_groups > 0 ? 2 * a.num_groups + 1 : 0) +
+                                      (sib ? 2 * a.num_sib + 1 : 0)
+                                : 0;
+  SmemLayout L = make_layout(4, tpu, hkv, D, elt, WH, G, a.num_seqs, 0);
+  if (L.total > smem_limit) L = make_layout(3, tpu, hkv, D, elt, WH, G, a.num_seqs, 0);
+  if (L.total > smem_limit) L = make_layout(2, tpu, hkv, D, elt, WH, G, a.num_seqs, 0);
   if (L.total > smem_limit) return cudaErrorInvalidValue;
+  if (meta_ints > 0) {
+    const SmemLayout Lm = make_layout(L.stages, tpu, hkv, D, elt, WH, G, a.num_seqs, meta_ints);
+    if (Lm.total <= smem_limit) L = Lm;
+  }
 
   int grid = a.grid_override > 0 ? a.grid_override : device_sm_count();
   grid = std::min(grid, kMaxDecodeCtas);
+  const int sib_m = sib ? 16 / G : 1;
+  const size_t slots = a.ws_slots > 0 ? a.ws_slots : static_cast<size_t>(kMaxDecodeCtas) + a.num_seqs;
+  // partial slots used: at most num_seqs + sib_m * grid
+  if (static_cast<size_t>(a.num_seqs) + static_cast<size_t>(sib_m) * grid > slots)
+    return cudaErrorInvalidValue;
 
   DecodeParams p;
   p.k_pool = static_cast<const char*>(a.pool.k);
@@ -1223,7 +1484,6 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * kLog2e;
   char* ws = static_cast<char*>(a.workspace);
   const size_t prefix_bytes = align_up_sz((a.num_seqs + 1) * 4, 256);
-  const size_t slots = static_cast<size_t>(kMaxDecodeCtas) + a.num_seqs;
   p.ws_prefix = reinterpret_cast<int*>(ws);
   p.ws_ml = reinterpret_cast<float2*>(ws + prefix_bytes);
   p.ws_acc = reinterpret_cast<float*>(ws + prefix_bytes + align_up_sz(slots * a.num_q_heads * 8, 256));
@@ -1235,6 +1495,12 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   p.pre_ml = static_cast<const float2*>(a.pre_ml);
   p.pre_acc = static_cast<const float*>(a.pre_acc);
   p.defer_prefix = a.defer_prefix;
+  p.cu_sib = sib ? a.cu_sib : nullptr;
+  p.shared_lens = sib ? a.shared_lens : nullptr;
+  p.num_sib = sib ? a.num_sib : 0;
+  p.sib_m = sib_m;
+  p.num_slots = static_cast<int64_t>(slots);
+  p.ws_rec = cascade ? static_cast<uint32_t*>(a.ws_rec) : nullptr;
   if constexpr (Cfg<T, D, G, WH>::kMma) {
     if (!make_tmap_pool_heads(&p.tm_k, a.pool.k, D, hkv, static_cast<uint64_t>(a.pool.num_blocks)) ||
         !make_tmap_pool_heads(&p.tm_v, a.pool.v, D, hkv, static_cast<uint64_t>(a.pool.num_blocks)))

@@ -63,8 +63,19 @@ struct DecodeArgs {
   const void* pre_acc;
   int defer_prefix;  // 1: the prefix partials are written concurrently; only the merge folds them
   int launch_part;   // 0: decode kernel and merge; 1: the decode kernel only; 2: the merge only
+  // nested cascade, second level (NULL / 0 otherwise): sequences cu_sib[j] ..
+  // cu_sib[j+1]-1 share their first shared_lens[j] tokens (whole blocks,
+  // including any first-level prefix); the tensor-core path reads those
+  // blocks once per entry of up to 16 / G members
+  const int32_t* cu_sib;
+  const int32_t* shared_lens;
+  int num_sib;
+  size_t ws_slots;   // partial slots the workspace holds (0: kMaxDecodeCtas + num_seqs)
+  void* ws_rec;      // cascade calls: [num_seqs] uint32 per-sequence records for the merge
 };
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim);
+// The same for a workspace of `slots` partial slots.
+size_t decode_workspace_bytes_slots(int num_seqs, int num_q_heads, int head_dim, size_t slots);
 // per (dtype, head_dim) entry points, one translation unit each
 cudaError_t decode_f32_d64(const DecodeArgs& a, int group, cudaStream_t stream);
 cudaError_t decode_f32_d128(const DecodeArgs& a, int group, cudaStream_t stream);

@@ -460,7 +460,7 @@ def shared_prefix_decode(seed: int = 0, num_requests: int = 256, replies: int = 
         scale=1.0 / math.sqrt(head_dim),
         token_budget=S,
         info={"seed": seed, "blocks_used": n_phys, "num_requests": num_requests,
-              "replies": replies, "shared_pages": n_shared},
+              "replies": replies, "shared_pages": n_shared, "prompt_len": prompt},
     )
 
 

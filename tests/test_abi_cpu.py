@@ -187,3 +187,32 @@ def test_cascade_validation(lib):
     sz = abi.pa_decode_cascade_workspace_size(768, 32, 128, 100)
     assert sz > abi.pa_decode_workspace_size(768, 32, 128, 100) + 768 * 32 * 128 * 4
     assert abi.pa_decode_cascade_workspace_size(-1, 32, 128, 100) == 0
+
+
+def nested(lib, pl, S=4, hq=8, mb=8, ng=1, nsib=1, sib=FAKE, slen=FAKE, ctas=0, ws=FAKE,
+           ws_bytes=1 << 40):
+    return lib.pa_decode_cascade_nested(ctypes.byref(pl), FAKE, FAKE, S, hq, FAKE, mb, FAKE, FAKE,
+                                        FAKE, ng, sib, slen, nsib, 0.125, ctas, ws, ws_bytes, None,
+                                        None)
+
+
+def test_nested_cascade_validation(lib):
+    # (checks that come before the support test, which needs the CUDA driver)
+    bf16 = dict(dtype=1, head_dim=128, num_kv_heads=2)
+    assert nested(lib, pool(**bf16), nsib=-1) == abi.PA_EINVAL
+    assert nested(lib, pool(**bf16), ng=-1) == abi.PA_EINVAL
+    assert nested(lib, pool(**bf16), ctas=-1) == abi.PA_EINVAL
+    assert nested(lib, pool(k=None, **bf16)) == abi.PA_EINVAL
+    assert nested(lib, pool(dtype=0, head_dim=128)) == abi.PA_EUNSUPPORTED
+    # an entry of up to 16 / G members that spans n CTAs leaves n partials per
+    # member: the partial slots grow to num_seqs + (16 / G) x CTAs
+    size = abi.pa_decode_cascade_nested_workspace_size
+    plain = abi.pa_decode_cascade_workspace_size(768, 32, 128, 100)
+    assert size(768, 32, 8, 128, 100, 0) > plain                      # G 4: 4 x 1024 slots
+    per_slot = 32 * (128 * 4 + 8)
+    assert size(768, 32, 8, 128, 100, 0) - size(768, 32, 8, 128, 100, 152) >= per_slot * 4 * (1024 - 152)
+    assert size(768, 32, 8, 128, 100, 152) < size(768, 32, 8, 128, 100, 0)
+    assert size(768, 64, 8, 128, 100, 152) > size(768, 32, 8, 128, 100, 152)
+    assert size(-1, 32, 8, 128, 100, 0) == 0
+    assert size(768, 30, 8, 128, 100, 0) == 0                          # heads not a multiple
+    assert size(768, 32, 8, 128, 100, -1) == 0
