@@ -163,7 +163,8 @@ struct SmemLayout {
   int parts;            // 16 / tokens_per_unit
   int part_bytes;       // one K (or V) part: tokens_per_unit * Hkv * D * elt
   int off_bars, off_done, off_flags, off_mbars, off_table, off_ntok, off_memb, off_merge, off_prefix,
-      off_meta;  // staged cascade metadata (0: not staged)
+      off_meta,   // staged cascade metadata (0: not staged)
+      off_info;   // per-sequence first block, shared blocks, record (0: not kept)
   int total;
 };
 
@@ -171,7 +172,7 @@ __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a *
 
 __host__ __device__ inline SmemLayout make_layout(int stages, int tokens_per_unit, int hkv, int d,
                                                   int elt, int wh, int group, int num_seqs,
-                                                  int meta_ints) {
+                                                  int meta_ints, bool info) {
   SmemLayout L;
   L.stages = stages;
   L.tokens_per_unit = tokens_per_unit;
@@ -190,7 +191,9 @@ __host__ __device__ inline SmemLayout make_layout(int stages, int tokens_per_uni
   L.off_prefix = align_up(L.off_merge + merge_bytes, 16);
   const int end = align_up(L.off_prefix + (num_seqs + 1) * 4, 16);
   L.off_meta = meta_ints > 0 ? end : 0;
-  L.total = align_up(end + meta_ints * 4, 128) + 1024;  // + base alignment
+  const int end2 = align_up(end + meta_ints * 4, 16);
+  L.off_info = info ? end2 : 0;
+  L.total = align_up(end2 + (info ? 3 * num_seqs * 4 : 0), 128) + 1024;  // + base alignment
   return L;
 }
 
@@ -293,102 +296,107 @@ __device__ __forceinline__ int entry_start(const P& p, int j, int s) {
   return g0 + (s - g0) / p.sib_m * p.sib_m;
 }
 
-// The entry (first member a, k members) of sequence s; (s, 1) outside every
-// sibling group.
-template <class P>
-__device__ __forceinline__ void entry_of(const P& p, int s, int* a, int* k) {
-  const int j = sib_group(p, s);
-  if (j < 0) {
-    *a = s;
-    *k = 1;
-    return;
-  }
-  *a = entry_start(p, j, s);
-  *k = min(p.sib_m, p.cu_sib[j + 1] - *a);
-}
-
 // The CTA whose range holds block b of the decode order (B blocks, `grid`
 // CTAs; CTA c holds blocks [c B / grid, (c + 1) B / grid)).
 __host__ __device__ __forceinline__ int64_t cta_of_block(int64_t b, int64_t B, int64_t grid) {
   return ((b + 1) * grid - 1) / B;
 }
 
-// Blocks the decode kernel reads for sequence s (0 when s is not a decode
-// sequence or its lengths are invalid). A sibling group's shared blocks after
-// the first-level prefix are counted once per entry, as blocks of its first
-// member; the other members count only their own blocks.
+// What the block walk needs to know about sequence s, worked out in one pass:
+// the blocks the decode kernel reads for it (0 when s is not a decode
+// sequence or its lengths are invalid), where they start in its block table,
+// and its sibling entry. A sibling group's shared blocks after the
+// first-level prefix are counted once per entry, as the first blocks of its
+// first member (every member's rows attend them); the other members count
+// only their own blocks.
+struct SeqInfo {
+  int blocks;   // blocks read for s
+  int first;    // logical block of s's table where they start
+  int nsh;      // how many of them are the entry's shared blocks
+  int off, k;   // s is member `off` of an entry of k members
+  bool bad;     // invalid lengths (the row is zeroed and flagged)
+  bool has_pre; // the attention over a first-level prefix is a separate partial
+};
 template <class P>
-__device__ __forceinline__ int decode_blocks(const P& p, int s, bool* bad) {
+__device__ __forceinline__ SeqInfo seq_info(const P& p, int s) {
+  SeqInfo r;
+  r.blocks = 0;
+  r.first = 0;
+  r.nsh = 0;
+  r.off = 0;
+  r.k = 1;
+  r.bad = false;
+  r.has_pre = false;
   int q_len = 1;
   if (p.cu_q_lens != nullptr) {
     q_len = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
     if (q_len < 0 || p.cu_q_lens[s] < 0 || p.cu_q_lens[s + 1] > p.num_rows) {
-      *bad = true;  // malformed cu_q_lens: never index q/out with it
-      return 0;
+      r.bad = true;  // malformed cu_q_lens: never index q/out with it
+      return r;
     }
   }
-  if (q_len != 1) return 0;
+  if (q_len != 1) return r;
   const int ctx = p.context_lens[s];
   if (ctx < 1 || ctx > p.max_blocks * kBlockSize) {
-    *bad = true;
-    return 0;
+    r.bad = true;
+    return r;
   }
   bool bad_prefix = false;
   const int skip = prefix_blocks(p, s, ctx, &bad_prefix);
   if (bad_prefix) {
-    *bad = true;
-    return 0;
+    r.bad = true;
+    return r;
   }
+  r.first = skip;
+  r.has_pre = skip > 0;
   const int j = sib_group(p, s);
-  if (j < 0) return (ctx + kBlockSize - 1) / kBlockSize - skip;
+  if (j < 0) {
+    r.blocks = (ctx + kBlockSize - 1) / kBlockSize - skip;
+    return r;
+  }
+  const int a = entry_start(p, j, s);
+  r.off = s - a;
+  r.k = min(p.sib_m, p.cu_sib[j + 1] - a);
   // the shared blocks are read through the entry's first member's table: its
   // lengths must hold them too, with the same first-level prefix
   const int shared = p.shared_lens[j];
   if (shared < skip * kBlockSize || shared % kBlockSize != 0 || shared > ctx) {
-    *bad = true;
-    return 0;
+    r.bad = true;
+    return r;
   }
-  const int a = entry_start(p, j, s);
   if (a != s) {
     const int ctx_a = p.context_lens[a];
     bool bad_a = false;
     if (ctx_a < 1 || ctx_a > p.max_blocks * kBlockSize || shared > ctx_a ||
         prefix_blocks(p, a, ctx_a, &bad_a) != skip || bad_a) {
-      *bad = true;
-      return 0;
+      r.bad = true;
+      return r;
     }
   }
-  const int own = (ctx + kBlockSize - 1) / kBlockSize - shared / kBlockSize;
-  return own + (a == s ? shared / kBlockSize - skip : 0);
+  const int se = shared / kBlockSize;
+  r.nsh = a == s ? se - skip : 0;
+  if (a != s) r.first = se;
+  r.blocks = (ctx + kBlockSize - 1) / kBlockSize - se + r.nsh;
+  return r;
 }
 
-// Where sequence s's blocks start in its block table (logical block `first`)
-// and which rows of its entry attend them: blocks before `shared_end` are the
-// sibling group's shared blocks (every member's rows), the rest are s's own.
-struct SeqWalk {
-  int first;
-  int shared_end;
-  uint32_t shared_mask;
-  uint32_t own_mask;
-};
+// SeqInfo packed for the merge kernel and the shared-memory table: bits 0-3
+// the member offset, 4-8 the entry size, 9 valid lengths, 10 a first-level
+// prefix partial.
+__device__ __forceinline__ uint32_t pack_rec(const SeqInfo& r) {
+  return static_cast<uint32_t>(r.off) | (static_cast<uint32_t>(r.k) << 4) | (r.bad ? 0u : 1u << 9) |
+         (r.has_pre ? 1u << 10 : 0u);
+}
+__device__ __forceinline__ int rec_off(uint32_t rec) { return static_cast<int>(rec & 15u); }
+__device__ __forceinline__ int rec_k(uint32_t rec) { return static_cast<int>((rec >> 4) & 31u); }
+__device__ __forceinline__ bool rec_valid(uint32_t rec) { return (rec >> 9) & 1u; }
+__device__ __forceinline__ bool rec_pre(uint32_t rec) { return (rec >> 10) & 1u; }
+
 template <class P>
-__device__ __forceinline__ SeqWalk seq_walk(const P& p, int s, int ctx) {
-  bool unused = false;
-  SeqWalk w;
-  w.first = prefix_blocks(p, s, ctx, &unused);
-  w.shared_end = 0;
-  w.shared_mask = 1u;
-  w.own_mask = 1u;
-  const int j = sib_group(p, s);
-  if (j >= 0) {
-    const int a = entry_start(p, j, s);
-    const int k = min(p.sib_m, p.cu_sib[j + 1] - a);
-    w.shared_end = p.shared_lens[j] / kBlockSize;
-    w.own_mask = 1u << (s - a);
-    if (a == s) w.shared_mask = (1u << k) - 1u;
-    else w.first = w.shared_end;
-  }
-  return w;
+__device__ __forceinline__ int decode_blocks(const P& p, int s, bool* bad) {
+  const SeqInfo r = seq_info(p, s);
+  if (r.bad) *bad = true;
+  return r.blocks;
 }
 
 __device__ __forceinline__ int query_row(const DecodeParams& p, int s) {
@@ -465,14 +473,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     int32_t* m_pl = m_cu + (p.num_groups > 0 ? p.num_groups + 1 : 0);
     int32_t* m_sib = m_pl + (p.num_groups > 0 ? p.num_groups : 0);
     int32_t* m_sl = m_sib + (p.num_sib > 0 ? p.num_sib + 1 : 0);
-    for (int i = tid; i < S; i += kThreads) m_ctx[i] = p.context_lens[i];
-    if (p.num_groups > 0) {
-      for (int i = tid; i <= p.num_groups; i += kThreads) m_cu[i] = p.cu_groups[i];
-      for (int i = tid; i < p.num_groups; i += kThreads) m_pl[i] = p.prefix_lens[i];
-    }
-    if (p.num_sib > 0) {
-      for (int i = tid; i <= p.num_sib; i += kThreads) m_sib[i] = p.cu_sib[i];
-      for (int i = tid; i < p.num_sib; i += kThreads) m_sl[i] = p.shared_lens[i];
+    // the five arrays lie back to back from m_ctx: one index space, eight
+    // loads in flight per thread before their stores (loads issued one by
+    // one would each wait out a round trip to a busy HBM)
+    const int n0 = S, n1 = static_cast<int>(m_pl - m_ctx), n2 = static_cast<int>(m_sib - m_ctx),
+              n3 = static_cast<int>(m_sl - m_ctx), n4 = n3 + (p.num_sib > 0 ? p.num_sib : 0);
+    auto src_at = [&](int i) -> int32_t {
+      if (i < n0) return __ldg(p.context_lens + i);
+      if (i < n1) return __ldg(p.cu_groups + (i - n0));
+      if (i < n2) return __ldg(p.prefix_lens + (i - n1));
+      if (i < n3) return __ldg(p.cu_sib + (i - n2));
+      return __ldg(p.shared_lens + (i - n3));
+    };
+    constexpr int kBatch = 8;
+    for (int base = 0; base < n4; base += kBatch * kThreads) {
+      int32_t v[kBatch];
+#pragma unroll
+      for (int r = 0; r < kBatch; ++r) {
+        const int i = base + r * kThreads + tid;
+        v[r] = i < n4 ? src_at(i) : 0;
+      }
+#pragma unroll
+      for (int r = 0; r < kBatch; ++r) {
+        const int i = base + r * kThreads + tid;
+        if (i < n4) m_ctx[i] = v[r];
+      }
     }
     if (tid == 0) {
       meta.context_lens = m_ctx;
@@ -498,33 +523,78 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     meta.sib_m = p.sib_m;
   }
   __syncthreads();
+  // Each sequence's SeqInfo, worked out once per CTA: kept in shared memory
+  // when it fits (then the block counts are scanned in place), else worked
+  // out again wherever it is needed.
+  int* s_first = L.off_info > 0 ? reinterpret_cast<int*>(smem + L.off_info) : nullptr;
+  int* s_nsh = s_first + S;
+  uint32_t* s_rec = reinterpret_cast<uint32_t*>(s_nsh + S);
   bool bad_len = false;
-  block_exclusive_scan<kThreads>(
-      S, [&](int s) { return decode_blocks(meta, s, &bad_len); }, prefix, warp_sums);
+  if (s_first != nullptr) {
+    const SeqMeta m = meta;  // in registers for the scan
+    for (int s = tid; s < S; s += kThreads) {
+      const SeqInfo r = seq_info(m, s);
+      prefix[s] = r.blocks;
+      s_first[s] = r.first;
+      s_nsh[s] = r.nsh;
+      s_rec[s] = pack_rec(r);
+      bad_len |= r.bad;
+    }
+    __syncthreads();
+    block_exclusive_scan<kThreads>(S, [&](int s) { return prefix[s]; }, prefix, warp_sums);
+  } else {
+    block_exclusive_scan<kThreads>(
+        S, [&](int s) { return decode_blocks(meta, s, &bad_len); }, prefix, warp_sums);
+  }
   if (bad_len && blockIdx.x == 0) status_or(p.d_status, PA_STATUS_BAD_LENGTH);
+  // the record of a sequence that has blocks to read: without groups or
+  // sibling groups it is the same for all (member 0 of a one-member entry,
+  // valid, no prefix partial), else kept or worked out again
+  const bool plain = p.cu_groups == nullptr && p.cu_sib == nullptr;
+  auto rec_of = [&](int s) -> uint32_t {
+    if (s_first != nullptr) return s_rec[s];
+    if (plain) return (1u << 4) | (1u << 9);
+    return pack_rec(seq_info(meta, s));
+  };
+  // logical block j of sequence s, and the rows of its entry that attend it,
+  // for block b of the decode order
+  auto locate = [&](int64_t b, int* s_out, int* j_out, uint32_t* rows_out) {
+    const int s = upper_index(prefix, S, b);
+    const int r = static_cast<int>(b - prefix[s]);
+    int first, nsh;
+    uint32_t rec;
+    if (s_first != nullptr) {
+      first = s_first[s];
+      nsh = s_nsh[s];
+      rec = s_rec[s];
+    } else if (plain) {  // the table lookup need not wait for the lengths
+      first = 0;
+      nsh = 0;
+      rec = rec_of(s);
+    } else {
+      const SeqInfo si = seq_info(meta, s);
+      first = si.first;
+      nsh = si.nsh;
+      rec = pack_rec(si);
+    }
+    *s_out = s;
+    *j_out = first + r;
+    *rows_out = r < nsh ? (1u << rec_k(rec)) - 1u : 1u << rec_off(rec);
+  };
 
   // cascade calls: the merge kernel's per-sequence record (see DecodeParams)
-  if (blockIdx.x == 0 && p.ws_rec != nullptr) {
-    for (int s = tid; s < S; s += kThreads) {
-      int a = s, k = 1;
-      entry_of(meta, s, &a, &k);
-      bool bad = false, pre_bad = false;
-      decode_blocks(meta, s, &bad);
-      const bool hp = prefix_blocks(meta, s, meta.context_lens[s], &pre_bad) > 0;
-      p.ws_rec[s] = static_cast<uint32_t>(s - a) | (static_cast<uint32_t>(k) << 4) |
-                    (bad ? 0u : 1u << 9) | (hp ? 1u << 10 : 0u);
-    }
-  }
+  if (blockIdx.x == 0 && p.ws_rec != nullptr)
+    for (int s = tid; s < S; s += kThreads)
+      p.ws_rec[s] = s_first != nullptr ? s_rec[s] : pack_rec(seq_info(meta, s));
 
   // Invalid decode sequences (bad lengths) get zero output rows, written once:
   // one warp of the grid checks each sequence, so no CTA lags the others
   for (int s = blockIdx.x * kWarps + warp; s < S; s += gridDim.x * kWarps) {
-    bool bad = false;
-    const bool decode_row = decode_blocks(meta, s, &bad) > 0 || bad;
+    const bool bad = s_first != nullptr ? !rec_valid(s_rec[s]) : seq_info(meta, s).bad;
     int q_len = 1;
     if (p.cu_q_lens != nullptr) q_len = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
     const int row = query_row(p, s);
-    if (decode_row && bad && q_len == 1 && row >= 0 && row < p.num_rows) {
+    if (bad && q_len == 1 && row >= 0 && row < p.num_rows) {
       T* o = static_cast<T*>(p.out) + static_cast<int64_t>(row) * p.hq * D;
       for (int i = lane; i < p.hq * D; i += 32) o[i] = from_float<T>(0.f);
     }
@@ -556,13 +626,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       block_tokens = block_ntok[rel];
       rows = block_memb[rel];
     } else {
-      const int s = upper_index(prefix, S, lo + rel);
-      const int ctx = meta.context_lens[s];
-      const SeqWalk sw = seq_walk(meta, s, ctx);
-      const int j = static_cast<int>(lo + rel - prefix[s]) + sw.first;  // logical block of s
+      int s, j;
+      locate(lo + rel, &s, &j, &rows);
       phys = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
-      block_tokens = min(kBlockSize, ctx - j * kBlockSize);
-      rows = j < sw.shared_end ? sw.shared_mask : sw.own_mask;
+      block_tokens = min(kBlockSize, meta.context_lens[s] - j * kBlockSize);
+      if (direct && rel < kTableCache) {  // staged here, not again below
+        table[rel] = phys;
+        block_ntok[rel] = static_cast<uint8_t>(block_tokens);
+        block_memb[rel] = static_cast<uint16_t>(rows);
+      }
     }
     memb[st] = rows;
     const int ntok = min(tpu, block_tokens - part * tpu);
@@ -598,20 +670,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // the first stages are issued from the global table at once, so their
   // copies are in flight while the CTA stages the rest of its table slice;
   // one thread each, so their table lookups overlap
-  if (tid < min(static_cast<int64_t>(L.stages), n_units)) issue(tid, tid, true);
-
+  const int n_first = static_cast<int>(min(static_cast<int64_t>(L.stages), n_units));
+  if (tid < n_first) issue(tid, tid, true);
 
   // stage this CTA's slice of the block tables (first kTableCache blocks)
-  // with the number of context tokens each block holds
+  // with the number of context tokens each block holds (the first n_first
+  // blocks were staged by their issue above; with parts > 1 a unit is a part
+  // of a block, and unit tid's block is tid / parts)
   const int n_cached = static_cast<int>(min(hi - lo, static_cast<int64_t>(kTableCache)));
-  for (int i = tid; i < n_cached; i += kThreads) {
-    const int s = upper_index(prefix, S, lo + i);
-    const int ctx = meta.context_lens[s];
-    const SeqWalk sw = seq_walk(meta, s, ctx);
-    const int j = static_cast<int>(lo + i - prefix[s]) + sw.first;
+  for (int i = tid + (parts == 1 && tid < n_first ? kThreads : 0); i < n_cached; i += kThreads) {
+    int s, j;
+    uint32_t rows;
+    locate(lo + i, &s, &j, &rows);
     table[i] = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
-    block_ntok[i] = static_cast<uint8_t>(min(kBlockSize, ctx - j * kBlockSize));
-    block_memb[i] = static_cast<uint16_t>(j < sw.shared_end ? sw.shared_mask : sw.own_mask);
+    block_ntok[i] = static_cast<uint8_t>(min(kBlockSize, meta.context_lens[s] - j * kBlockSize));
+    block_memb[i] = static_cast<uint16_t>(rows);
   }
   __syncthreads();
   // the merge kernel may be launched now: it waits (griddepcontrol.wait) for
@@ -654,8 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     while (u < n_units && ok) {
       while (prefix[s + 1] <= lo + (parts == 1 ? u : u / parts)) ++s;
       // the entry holding s: members a .. a + k - 1, blocks [e_lo, e_hi)
-      int a = s, k = 1;
-      if (p.cu_sib != nullptr) entry_of(meta, s, &a, &k);
+      const uint32_t rec_s = rec_of(s);
+      const int a = s - rec_off(rec_s), k = rec_k(rec_s);
       const int64_t e_lo = prefix[a], e_hi = prefix[a + k];
       // units from here to the end of the entry or of the range (counted from
       // the current unit, so that even inconsistent sibling bounds cannot
@@ -669,12 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       {
         bool v = false, hp = false;
         if (lane < k) {
-          const int sq = a + lane;
-          bool bad = false;
-          if (k > 1) decode_blocks(meta, sq, &bad);
-          v = !bad;
-          bool pre_bad = false;
-          hp = prefix_blocks(meta, sq, meta.context_lens[sq], &pre_bad) > 0;
+          const uint32_t rm = rec_of(a + lane);
+          v = rec_valid(rm);
+          hp = rec_pre(rm);
         }
         vmask = __ballot_sync(0xffffffffu, v);
         pmask = __ballot_sync(0xffffffffu, hp);
@@ -903,8 +973,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int64_t seq_units = (seq_hi - seq_lo) * parts;
     const bool whole = prefix[s] >= lo && prefix[s + 1] <= hi;
     const int row = query_row(p, s);
-    bool pre_bad = false;
-    const bool has_pre = prefix_blocks(meta, s, meta.context_lens[s], &pre_bad) > 0;
+    const bool has_pre = rec_pre(rec_of(s));
 
     // this lane's query heads, pre-scaled into the log2 domain
     {
@@ -1450,13 +1519,21 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   const int meta_ints = cascade ? a.num_seqs + (a.num_groups > 0 ? 2 * a.num_groups + 1 : 0) +
                                       (sib ? 2 * a.num_sib + 1 : 0)
                                 : 0;
-  SmemLayout L = make_layout(4, tpu, hkv, D, elt, WH, G, a.num_seqs, 0);
-  if (L.total > smem_limit) L = make_layout(3, tpu, hkv, D, elt, WH, G, a.num_seqs, 0);
-  if (L.total > smem_limit) L = make_layout(2, tpu, hkv, D, elt, WH, G, a.num_seqs, 0);
+  SmemLayout L = make_layout(4, tpu, hkv, D, elt, WH, G, a.num_seqs, 0, false);
+  if (L.total > smem_limit) L = make_layout(3, tpu, hkv, D, elt, WH, G, a.num_seqs, 0, false);
+  if (L.total > smem_limit) L = make_layout(2, tpu, hkv, D, elt, WH, G, a.num_seqs, 0, false);
   if (L.total > smem_limit) return cudaErrorInvalidValue;
-  if (meta_ints > 0) {
-    const SmemLayout Lm = make_layout(L.stages, tpu, hkv, D, elt, WH, G, a.num_seqs, meta_ints);
-    if (Lm.total <= smem_limit) L = Lm;
+  // beside the stages, for a cascade call and when they fit: its staged
+  // metadata and the per-sequence facts, else the facts alone (a plain
+  // decode's prologue is shorter without them)
+  if (cascade) {
+    for (const int m : {meta_ints, 0}) {
+      const SmemLayout Li = make_layout(L.stages, tpu, hkv, D, elt, WH, G, a.num_seqs, m, true);
+      if (Li.total <= smem_limit) {
+        L = Li;
+        break;
+      }
+    }
   }
 
   int grid = a.grid_override > 0 ? a.grid_override : device_sm_count();

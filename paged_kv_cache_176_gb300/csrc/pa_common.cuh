@@ -186,7 +186,9 @@ __device__ __forceinline__ void pdl_wait_primary() {
 
 // Block-wide exclusive scan of count(i) over items i in [0, n): prefix[i] for
 // i < n and prefix[n] = total. kThreads threads; warp_sums holds kThreads/32
-// ints of shared memory. Ends with __syncthreads().
+// ints of shared memory. Ends with __syncthreads(). count(i) may read
+// prefix[i] (a scan in place): thread t reads and writes only its own items,
+// and reads each before writing it.
 template <int kThreads, typename CountFn>
 __device__ void block_exclusive_scan(int n, CountFn count, int* prefix, int* warp_sums) {
   constexpr int kW = kThreads / 32;
@@ -216,8 +218,9 @@ __device__ void block_exclusive_scan(int n, CountFn count, int* prefix, int* war
   __syncthreads();
   int run = incl - sum + (warp > 0 ? warp_sums[warp - 1] : 0);
   for (int i = lo; i < hi; ++i) {
+    const int c = count(i);
     prefix[i] = run;
-    run += count(i);
+    run += c;
   }
   if (tid == kThreads - 1) prefix[n] = run;
   __syncthreads();
