@@ -428,9 +428,13 @@ __device__ __forceinline__ float merge_factor(float m, float mn) {
   return m == -INFINITY ? 0.f : fast_exp2(m - mn);
 }
 
-template <typename T, int D, int G, int WH>
+// kSib: the nested cascade's sibling entries (tensor-core path only); the
+// other instantiation walks one sequence per entry with none of their
+// bookkeeping (row masks, member records, entry slots) in its loops.
+template <typename T, int D, int G, int WH, bool kSib>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = Cfg<T, D, G, WH>;
+  static_assert(!kSib || C::kMma, "sibling entries run on the tensor-core path");
   constexpr int HKV = C::kHkv;
   extern __shared__ __align__(128) char smem_raw[];
   // 1024-byte aligned base (128-byte swizzled TMA boxes need it)
@@ -527,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // when it fits (then the block counts are scanned in place), else worked
   // out again wherever it is needed.
   int* s_first = L.off_info > 0 ? reinterpret_cast<int*>(smem + L.off_info) : nullptr;
-  int* s_nsh = s_first + S;
-  uint32_t* s_rec = reinterpret_cast<uint32_t*>(s_nsh + S);
+  int* s_nsh = L.off_info > 0 ? s_first + S : nullptr;
+  uint32_t* s_rec = L.off_info > 0 ? reinterpret_cast<uint32_t*>(s_nsh + S) : nullptr;
   bool bad_len = false;
   if (s_first != nullptr) {
     const SeqMeta m = meta;  // in registers for the scan
@@ -624,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (rel < kTableCache && !direct) {
       phys = table[rel];
       block_tokens = block_ntok[rel];
-      rows = block_memb[rel];
+      rows = kSib ? block_memb[rel] : 1u;
     } else {
       int s, j;
       locate(lo + rel, &s, &j, &rows);
@@ -633,10 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       if (direct && rel < kTableCache) {  // staged here, not again below
         table[rel] = phys;
         block_ntok[rel] = static_cast<uint8_t>(block_tokens);
-        block_memb[rel] = static_cast<uint16_t>(rows);
+        if constexpr (kSib) block_memb[rel] = static_cast<uint16_t>(rows);
       }
     }
-    memb[st] = rows;
+    if constexpr (kSib) memb[st] = rows;
     const int ntok = min(tpu, block_tokens - part * tpu);
     if (phys < 0 || phys >= p.num_blocks) {
       flags[st] = -1;
@@ -684,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     locate(lo + i, &s, &j, &rows);
     table[i] = p.block_tables[static_cast<int64_t>(s) * p.max_blocks + j];
     block_ntok[i] = static_cast<uint8_t>(min(kBlockSize, meta.context_lens[s] - j * kBlockSize));
-    block_memb[i] = static_cast<uint16_t>(rows);
+    if constexpr (kSib) block_memb[i] = static_cast<uint16_t>(rows);
   }
   __syncthreads();
   // the merge kernel may be launched now: it waits (griddepcontrol.wait) for
@@ -728,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       while (prefix[s + 1] <= lo + (parts == 1 ? u : u / parts)) ++s;
       // the entry holding s: members a .. a + k - 1, blocks [e_lo, e_hi)
       const uint32_t rec_s = rec_of(s);
-      const int a = s - rec_off(rec_s), k = rec_k(rec_s);
+      const int a = kSib ? s - rec_off(rec_s) : s, k = kSib ? rec_k(rec_s) : 1;
       const int64_t e_lo = prefix[a], e_hi = prefix[a + k];
       // units from here to the end of the entry or of the range (counted from
       // the current unit, so that even inconsistent sibling bounds cannot
@@ -738,8 +742,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       // members with valid lengths (a member with bad ones may sit in an
       // entry whose shared blocks are read; its row stays zero) and members
       // with a first-level prefix partial, one lane per member
-      uint32_t vmask, pmask;
-      {
+      uint32_t vmask = 1u, pmask = rec_pre(rec_s) ? 1u : 0u;
+      if constexpr (kSib) {
         bool v = false, hp = false;
         if (lane < k) {
           const uint32_t rm = rec_of(a + lane);
@@ -750,7 +754,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         pmask = __ballot_sync(0xffffffffu, hp);
       }
       // Q as stored (bf16 pairs); the scale is applied to the fp32 scores
-      {
+      if constexpr (!kSib) {
+        const uint32_t* q = reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) +
+                                                              static_cast<int64_t>(query_row(p, s)) * p.hq * D);
+        const int h0 = g * G + gi, h1 = g * G + gi + 8;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const int c = (16 * kk + 2 * qi) / 2;  // bf16-pair index
+          qa[kk][0] = gi < G ? __ldg(q + h0 * (D / 2) + c) : 0u;
+          qa[kk][1] = gi + 8 < G ? __ldg(q + h1 * (D / 2) + c) : 0u;
+          qa[kk][2] = gi < G ? __ldg(q + h0 * (D / 2) + c + 4) : 0u;
+          qa[kk][3] = gi + 8 < G ? __ldg(q + h1 * (D / 2) + c + 4) : 0u;
+        }
+      } else {
         const bool in0 = mr0 < k, in1 = mr1 < k;
         const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
             static_cast<const T*>(p.q) + static_cast<int64_t>(query_row(p, a + (in0 ? mr0 : 0))) * p.hq * D);
@@ -768,7 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-      float m0 = kNoMax, m1 = kNoMax, l0 = 0.f, l1 = 0.f;
+      // a sibling entry's rows start from a finite running max (kNoMax)
+      float m0 = kSib ? kNoMax : -INFINITY, m1 = kSib ? kNoMax : -INFINITY, l0 = 0.f, l1 = 0.f;
       uint32_t poison = 0;  // members whose rows met a bad block
 
       for (int su = 0; su < seq_units; ++su, ++u) {
@@ -776,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], ph_c));
         if (!ok) break;
         const int ntok = flags[st];
-        if (ntok < 0) poison |= memb[st];
+        if (ntok < 0) poison |= kSib ? memb[st] : 1u;
         if (ntok > 0) {
           const uint32_t kb = sbase + static_cast<uint32_t>(st * 2 * L.part_bytes);
           const uint32_t vb = kb + static_cast<uint32_t>(L.part_bytes);
@@ -807,8 +824,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           // log2-domain scores; tokens past the context, and every token for
           // rows of members that do not attend this block (another member's
           // own block), are masked
-          const uint32_t rows = memb[st];
-          const int nt0 = (rows >> mr0) & 1u ? ntok : 0, nt1 = (rows >> mr1) & 1u ? ntok : 0;
+          int nt0 = ntok, nt1 = ntok;
+          if constexpr (kSib) {
+            const uint32_t rows = memb[st];
+            nt0 = (rows >> mr0) & 1u ? ntok : 0;
+            nt1 = (rows >> mr1) & 1u ? ntok : 0;
+          }
           float mt0 = -INFINITY, mt1 = -INFINITY;
 #pragma unroll
           for (int n = 0; n < 2; ++n)
@@ -829,7 +850,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           const bool need0 = mt0 > m0 + kRescaleThreshold, need1 = mt1 > m1 + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need0 || need1)) {
             const float n0 = need0 ? mt0 : m0, n1 = need1 ? mt1 : m1;
-            const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);  // 0 from kNoMax
+            // 0 from -inf (plain) or kNoMax (sibling entries)
+            const float a0 = (!kSib && m0 == -INFINITY) ? 0.f : fast_exp2(m0 - n0);
+            const float a1 = (!kSib && m1 == -INFINITY) ? 0.f : fast_exp2(m1 - n1);
             l0 *= a0;
             l1 *= a1;
 #pragma unroll
@@ -891,8 +914,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       // writes slot a + c_f sib_m + m n_c + (c - c_f), unique over the batch
       // since entries and CTA ranges are both in block order (c + s without
       // sibling groups)
-      const int64_t c_f = cta_of_block(e_lo, prefix[S], gridDim.x);
-      const int64_t n_c = cta_of_block(e_hi - 1, prefix[S], gridDim.x) - c_f + 1;
+      int64_t slot_c = static_cast<int64_t>(blockIdx.x) + s, n_c = 0;  // member 0's slot
+      if constexpr (kSib) {
+        const int64_t c_f = cta_of_block(e_lo, prefix[S], gridDim.x);
+        n_c = cta_of_block(e_hi - 1, prefix[S], gridDim.x) - c_f + 1;
+        slot_c = a + c_f * p.sib_m + (static_cast<int64_t>(blockIdx.x) - c_f);
+      }
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int mr = r ? mr1 : mr0;  // member of the entry
@@ -929,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           for (int n = 0; n < D / 8; ++n)
             orow[4 * n + qi] = pack_bf16x2(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
         } else {
-          const int64_t slot = a + c_f * p.sib_m + mr * n_c + (static_cast<int64_t>(blockIdx.x) - c_f);
+          const int64_t slot = slot_c + mr * n_c;
           if (slot < 0 || slot >= p.num_slots) continue;  // only with inconsistent sibling bounds
           if (qi == 0) p.ws_ml[slot * p.hq + head] = make_float2(mx, poisoned ? -1.f : lr_);
           float* arow = p.ws_acc + (slot * p.hq + head) * D;
@@ -1584,7 +1611,10 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
 
-  auto kern = decode_kernel<T, D, G, WH>;
+  auto kern = decode_kernel<T, D, G, WH, false>;
+  if constexpr (Cfg<T, D, G, WH>::kMma) {
+    if (sib) kern = decode_kernel<T, D, G, WH, true>;
+  }
   if (a.launch_part != 2) {
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
