@@ -216,3 +216,25 @@ def test_nested_cascade_bad_lengths_zeroed():
     first = 15 + G * ((23 - 15) // G)
     assert first == 23
     check(list(NESTED_SIB_LENS), {17: 390, 23: 395}, {17, 23, 24, 25, 26})
+
+
+@pytest.mark.parametrize("ctas", [0, 7])
+def test_nested_cascade_bad_block_zeroed(ctas):
+    """A bad block ID among an entry's shared blocks (read through its first
+    member's table) zeroes every member of that entry; one among a member's
+    own blocks zeroes that member alone. Both are flagged, the rest exact."""
+    w = nested_workload(32, 8)
+    ref = oracle_out(w)
+    db = to_device(w)
+    # entry [15, 19) of the sibling group [15, 30): shared blocks 10 .. 24
+    # (160-token first-level prefix, 400 shared tokens), read through 15
+    db.block_tables[15, 12] = w.num_blocks + 5
+    # entry [19, 23): member 20 (470 tokens) has own blocks 25 .. 29
+    assert int(w.context_lens[20]) == 470
+    db.block_tables[20, 27] = w.num_blocks + 7
+    out, db = run_nested(w, NESTED_CU_GROUPS, NESTED_PREFIX, NESTED_CU_SIB, NESTED_SIB_LENS,
+                         db=db, ctas=ctas)
+    assert int(db.status.item()) & pa.abi.PA_STATUS_BAD_BLOCK
+    zero = [15, 16, 17, 18, 20]
+    assert torch.count_nonzero(out[zero]) == 0
+    compare(out, ref, torch.bfloat16, rows=[s for s in range(48) if s not in zero])
