@@ -49,6 +49,13 @@
 //    a batch are reduce-scattered over the lanes of a token group, so each
 //    score's max, weight and sum are computed by one lane only, and the
 //    weights are gathered back for P.V.
+//  * Two-level cascade (kSib instantiation): a sibling group's members (a
+//    request's replies) are walked in entries of up to 16 / G, their query
+//    rows packed into the 16-row tile; an entry's shared blocks are read and
+//    multiplied once for all of its members, each member's own blocks with
+//    the other rows masked. Partials of member m of an entry starting at
+//    sequence a, in CTA c of the entry's CTAs c_f .. c_f + n_c - 1, go to slot
+//    a + c_f (16 / G) + m n_c + (c - c_f) (c + s without siblings).
 //  * Tokens past the context (the tail of a last block) are never loaded by
 //    the CUDA-core path; the tensor-core path loads the whole block, masks
 //    their scores and zeroes their value rows in shared memory. Either way
@@ -392,6 +399,7 @@ __device__ __forceinline__ int rec_k(uint32_t rec) { return static_cast<int>((re
 __device__ __forceinline__ bool rec_valid(uint32_t rec) { return (rec >> 9) & 1u; }
 __device__ __forceinline__ bool rec_pre(uint32_t rec) { return (rec >> 10) & 1u; }
 
+// Blocks the decode kernel reads for sequence s; sets *bad for invalid lengths.
 template <class P>
 __device__ __forceinline__ int decode_blocks(const P& p, int s, bool* bad) {
   const SeqInfo r = seq_info(p, s);
