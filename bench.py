@@ -57,8 +57,8 @@ SPEC_BF16_TFLOPS = 2250.0    # dense bf16 tensor
 # DRAM bytes (read + write) of one pa_decode call (decode_kernel +
 # decode_reduce_kernel) on the decode batch, from an ncu capture of
 # `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`, valid for the
-# kernel source whose sha256 prefix is given; reported as null once the
-# source changes.
+# kernel code whose sha256 prefix is given (see _src_sha); reported as null
+# once the code changes.
 NCU_DECODE_TRAFFIC = {"bytes": 643708672, "src_sha": "4a2700682b49f2bc"}
 
 
