@@ -309,6 +309,21 @@ class Scheduler:
         return {k: int(x.value) for k, x in zip(keys, v)}
 
 
+def sibling_shared_tokens(tables, context_lens, block_size: int = 16) -> int:
+    """Tokens a group of sequences (a request's beams or sampled replies) can
+    share in pa_decode_cascade_nested: the leading block-table entries equal
+    in every row (the same physical blocks, so the same cache contents),
+    whole pages only, each within every member's context."""
+    t = np.asarray(tables)
+    c = np.asarray(context_lens)
+    if t.shape[0] == 0:
+        return 0
+    lim = min(int(c.min()) // block_size, t.shape[1])
+    eq = np.all(t[:, :lim] == t[0, :lim], axis=0)
+    n = lim if bool(eq.all()) else int(np.argmin(eq))
+    return n * block_size
+
+
 def pa_reshape_and_cache_cow(k_pool, v_pool, k_new, v_new, slot_mapping, cow_src, cow_dst,
                              cow_ntok, d_status=None, stream=None) -> None:
     """KV write of the step's tokens with the copy-on-write copies (the filled

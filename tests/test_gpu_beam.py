@@ -8,7 +8,8 @@ import torch
 
 import oracle
 import paged_kv_cache_176_gb300 as pa
-from paged_kv_cache_176_gb300.serving import BlockManager, pa_reshape_and_cache_cow
+from paged_kv_cache_176_gb300.serving import (BlockManager, pa_reshape_and_cache_cow,
+                                              sibling_shared_tokens)
 from parity import compare
 
 pytestmark = pytest.mark.gpu
@@ -116,3 +117,78 @@ def test_beam_search_decode_matches_oracle(dtype, hq, hkv, d):
     for b in beams:
         bm.free(b)
     assert bm.num_free == nb
+
+
+@pytest.mark.parametrize("B", [4, 6])
+def test_beam_search_nested_cascade_decode(B):
+    """Beam search decoded with pa_decode_cascade_nested, each request's beams
+    one sibling group whose shared length is the pages their block tables
+    have in common: the shared pages are read once per entry of 4 beams (bf16,
+    32/8 heads: 16/4 rows per tile; 6 beams make entries of 4 and 2), and
+    the result matches the oracle and pa_decode. Two requests, so the groups
+    sit side by side in one batch."""
+    dtype, hq, hkv, d = torch.bfloat16, 32, 8, 128
+    R, steps, prompt, nb = 2, 24, 300, 256
+    g = torch.Generator().manual_seed(11)
+    rng = np.random.default_rng(12)
+    hk = torch.full((nb, 16, hkv, d), float("nan"), dtype=dtype)
+    hv = hk.clone()
+    dk, dv = hk.cuda(), hv.cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = d ** -0.5
+    bm = BlockManager(nb)
+    beams, next_id = [], 0
+    for r in range(R):
+        bm.add(next_id)
+        slots, _ = bm.append(next_id, prompt + 7 * r)
+        kn = torch.randn(len(slots), hkv, d, generator=g).to(dtype)
+        vn = torch.randn(len(slots), hkv, d, generator=g).to(dtype)
+        pa_reshape_and_cache_cow(dk, dv, kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda(), None,
+                                 None, None, d_status=st)
+        _host_apply(hk, hv, kn, vn, slots.tolist(), [])
+        beams.append([next_id])
+        next_id += 1
+    shared_seen = 0
+    for step in range(steps):
+        slots, cows, order = [], [], []
+        for r in range(R):
+            parents = rng.integers(0, len(beams[r]), size=B)
+            new = list(range(next_id, next_id + B))
+            next_id += B
+            bm.beam_step(beams[r], parents, new)
+            beams[r] = new
+            for b in new:
+                s_, c_ = bm.append(b, 1)
+                slots.append(int(s_[0]))
+                cows += c_
+                order.append(b)
+        S = len(order)
+        kn = torch.randn(S, hkv, d, generator=g).to(dtype)
+        vn = torch.randn(S, hkv, d, generator=g).to(dtype)
+        src, dst, ntok = (_i32([c[i] for c in cows]) if cows else None for i in range(3))
+        pa_reshape_and_cache_cow(dk, dv, kn.cuda(), vn.cuda(), torch.tensor(slots, device="cuda"),
+                                 src, dst, ntok, d_status=st)
+        _host_apply(hk, hv, kn, vn, slots, cows)
+        ctx = [bm.num_tokens(b) for b in order]
+        mb = max((c + 15) // 16 for c in ctx)
+        tables = torch.full((S, mb), -1, dtype=torch.int32)
+        for i, b in enumerate(order):
+            t = bm.block_table(b)
+            tables[i, :len(t)] = torch.from_numpy(t)
+        lens = [sibling_shared_tokens(tables[r * B:(r + 1) * B].numpy(), ctx[r * B:(r + 1) * B])
+                for r in range(R)]
+        shared_seen += sum(lens)
+        q = torch.randn(S, hq, d, generator=g).to(dtype)
+        out = torch.empty(S, hq, d, dtype=dtype, device="cuda")
+        pa.pa_decode_cascade_nested(out, q.cuda(), dk, dv, tables.cuda(), _i32(ctx), _i32([0]),
+                                    _i32([]), _i32([r * B for r in range(R + 1)]), _i32(lens),
+                                    scale, d_status=st)
+        plain = torch.empty_like(out)
+        pa.pa_decode(plain, q.cuda(), dk, dv, tables.cuda(), _i32(ctx), scale, d_status=st)
+        torch.cuda.synchronize()
+        ref = oracle.paged_attention(q, hk, hv, torch.arange(S + 1, dtype=torch.int32),
+                                     torch.tensor(ctx, dtype=torch.int32), tables, scale)
+        compare(out, ref, dtype)
+        compare(plain, ref, dtype)
+    assert int(st.item()) == 0
+    assert shared_seen >= steps * R * (prompt // 16) * 16  # the prompt pages at least

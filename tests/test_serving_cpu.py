@@ -190,3 +190,33 @@ def test_scheduler_rejects_impossible_request():
     assert e.value.status == PA_ENOSPACE
     with pytest.raises(abi.PagedAttentionError):
         sched.submit(2, 0, 1)
+
+
+def test_sibling_shared_tokens():
+    from paged_kv_cache_176_gb300.serving import sibling_shared_tokens as shared
+    t = np.array([[5, 6, 7, 8, 9], [5, 6, 7, 3, 4], [5, 6, 7, 8, 2]])
+    assert shared(t, [80, 70, 75]) == 48            # 3 equal leading blocks
+    assert shared(t, [80, 40, 75]) == 32            # only whole pages within every context
+    assert shared(t[:1], [70]) == 64                # one member: its whole pages
+    assert shared(t, [15, 70, 75]) == 0             # a member inside its first page
+    assert shared(np.array([[1, 2], [9, 2]]), [32, 32]) == 0
+    assert shared(np.zeros((0, 4), dtype=np.int32), []) == 0
+
+
+def test_sibling_shared_tokens_on_beams():
+    """Beams forked from one prompt share its full pages and, after a fork,
+    every page their parent had filled; the helper finds exactly the pages
+    the block manager shares (refcount equal to the number of beams)."""
+    from paged_kv_cache_176_gb300.serving import sibling_shared_tokens as shared
+    bm = BlockManager(64)
+    bm.add(0)
+    bm.append(0, 70)                                 # 4 full pages + 6 tokens
+    bm.beam_step([0], [0, 0, 0], [1, 2, 3])
+    for b in (1, 2, 3):
+        bm.append(b, 1)                              # copy-on-write of the partial page
+    rows = [bm.block_table(b) for b in (1, 2, 3)]
+    ctx = [bm.num_tokens(b) for b in (1, 2, 3)]
+    n = shared(np.stack([r[:5] for r in rows]), ctx)
+    assert n == 64
+    assert all(bm.refcount(int(rows[0][j])) == 3 for j in range(n // 16))
+    assert bm.refcount(int(rows[0][4])) == 1
