@@ -1423,31 +1423,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 }
 
 // Merge the partials of sequences that straddle CTAs: o = sum_c a_c acc_c /
-// sum_c a_c l_c with a_c = 2^(m_c - max_c m_c). One warp per (sequence,
-// head), eight per CTA, so every partial of the batch is read at once;
-// partials are read four at a time so their loads overlap.
-template <typename T, int D>
+// sum_c a_c l_c with a_c = 2^(m_c - max_c m_c). One warp per (sequence, kHpw
+// heads), eight per CTA: the sequence's lookups (record, block range, slots)
+// are done once for its heads, and the partials of every head and of four
+// CTAs at a time are loaded before any is used, so their latencies overlap.
+// kHpw = 1 for small batches (then every row of the batch is read at once),
+// more for large ones (fewer warps, fewer waves).
+template <typename T, int D, int kHpw>
 __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p, int grid) {
   pdl_wait_primary();
   constexpr int kPer = D / 32;  // elements per lane
+  const int hgroups = p.hq / kHpw;
   const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (item >= p.num_seqs * p.hq) return;
-  const int s = item / p.hq, h = item % p.hq;
+  if (item >= p.num_seqs * hgroups) return;
+  const int s = item / hgroups, h0 = (item % hgroups) * kHpw;
   const int lane = threadIdx.x & 31;
-  // cascade decode: this row's prefix partial, loaded first (its address
-  // depends on nothing else, and in-bounds for every row) so that its latency
-  // overlaps the lookups below; used only when the row has a prefix
-  float2 pml = make_float2(-INFINITY, 0.f);
-  float pacc[kPer];
-  if (p.cu_groups != nullptr) {
-    const int64_t idx = static_cast<int64_t>(s) * p.hq + h;
-    pml = p.pre_ml[idx];
-    const float* src = p.pre_acc + idx * D + lane * kPer;
+  // cascade decode: these rows' prefix partials, loaded first (their
+  // addresses depend on nothing else, and are in bounds for every row) so
+  // that their latency overlaps the lookups below; used only with a prefix
+  float2 pml[kHpw];
+  float pacc[kHpw][kPer];
 #pragma unroll
-    for (int e = 0; e < kPer; e += 2) {
-      const float2 x = *reinterpret_cast<const float2*>(src + e);
-      pacc[e] = x.x;
-      pacc[e + 1] = x.y;
+  for (int q = 0; q < kHpw; ++q) pml[q] = make_float2(-INFINITY, 0.f);
+  if (p.cu_groups != nullptr) {
+#pragma unroll
+    for (int q = 0; q < kHpw; ++q) {
+      const int64_t idx = static_cast<int64_t>(s) * p.hq + h0 + q;
+      pml[q] = p.pre_ml[idx];
+      const float* src = p.pre_acc + idx * D + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; e += 2) {
+        const float2 x = *reinterpret_cast<const float2*>(src + e);
+        pacc[q][e] = x.x;
+        pacc[q][e + 1] = x.y;
+      }
     }
   }
   // the entry holding s (members ea .. ea + ek - 1; s alone without sibling
@@ -1476,22 +1485,28 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
   } else if (!has_pre) {
     return;  // not a decode sequence, zeroed by the decode kernel, or nothing to merge
   }
-  float m = -INFINITY, l = 0.f;
-  float acc[kPer];
+  float m[kHpw], l[kHpw];
+  float acc[kHpw][kPer];
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  for (int q = 0; q < kHpw; ++q) {
+    m[q] = -INFINITY;
+    l[q] = 0.f;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[q][e] = 0.f;
+  }
   bool poisoned = false;
   // with at least as many blocks as CTAs no CTA range is empty: skip the test
   const bool all_nonempty = B >= grid;
   // this member's partial of CTA c sits at slot0 + c (see the decode kernel)
   const int64_t slot0 = ea + c_first * p.sib_m + static_cast<int64_t>(s - ea) * (c_last - c_first + 1) -
                         c_first;
-  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
-    float2 ml[4];
-    float v[4][kPer];
-    bool use[4];
+  constexpr int kC = kHpw > 1 ? 1 : 4;  // CTAs per batch of loads (registers: two CTAs per SM at kHpw 4)
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += kC) {
+    float2 ml[kHpw][kC];
+    float v[kHpw][kC][kPer];
+    bool use[kC];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kC; ++j) {
       const int64_t c = c0 + j;
       use[j] = c <= c_last && (all_nonempty || c * B / grid != (c + 1) * B / grid);
       if (use[j] && (slot0 + c < 0 || slot0 + c >= p.num_slots)) {
@@ -1499,40 +1514,53 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
         poisoned = true;
       }
       if (use[j]) {
-        ml[j] = p.ws_ml[(slot0 + c) * p.hq + h];
-        const float* src = p.ws_acc + ((slot0 + c) * p.hq + h) * D + lane * kPer;
 #pragma unroll
-        for (int e = 0; e < kPer; e += 2) {
-          const float2 x = *reinterpret_cast<const float2*>(src + e);
-          v[j][e] = x.x;
-          v[j][e + 1] = x.y;
+        for (int q = 0; q < kHpw; ++q) {
+          ml[q][j] = p.ws_ml[(slot0 + c) * p.hq + h0 + q];
+          const float* src = p.ws_acc + ((slot0 + c) * p.hq + h0 + q) * D + lane * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; e += 2) {
+            const float2 x = *reinterpret_cast<const float2*>(src + e);
+            v[q][j][e] = x.x;
+            v[q][j][e + 1] = x.y;
+          }
         }
       }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kC; ++j) {
       if (!use[j]) continue;
-      poisoned |= ml[j].y < 0.f;
-      const float mn = fmaxf(m, ml[j].x);
-      const float a = merge_factor(m, mn), b = merge_factor(ml[j].x, mn);
-      l = l * a + ml[j].y * b;
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) acc[e] = acc[e] * a + v[j][e] * b;
-      m = mn;
+      for (int q = 0; q < kHpw; ++q) {
+        poisoned |= ml[q][j].y < 0.f;
+        const float mn = fmaxf(m[q], ml[q][j].x);
+        const float a = merge_factor(m[q], mn), b = merge_factor(ml[q][j].x, mn);
+        l[q] = l[q] * a + ml[q][j].y * b;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) acc[q][e] = acc[q][e] * a + v[q][j][e] * b;
+        m[q] = mn;
+      }
     }
   }
-  if (has_pre) {
-    poisoned |= pml.y < 0.f;
-    const float mn = fmaxf(m, pml.x);
-    const float a = merge_factor(m, mn), b = merge_factor(pml.x, mn);
-    l = l * a + pml.y * b;
+  // a poisoned partial (a bad block) zeroes the whole row: one poisoned
+  // head's partial means its CTA met the block for every head of the sequence
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = acc[e] * a + pacc[e] * b;
+  for (int q = 0; q < kHpw; ++q) {
+    bool pois = poisoned;
+    if (has_pre) {
+      pois |= pml[q].y < 0.f;
+      const float mn = fmaxf(m[q], pml[q].x);
+      const float a = merge_factor(m[q], mn), b = merge_factor(pml[q].x, mn);
+      l[q] = l[q] * a + pml[q].y * b;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) acc[q][e] = acc[q][e] * a + pacc[q][e] * b;
+    }
+    const float inv = pois ? 0.f : 1.f / l[q];
+    T* dst = static_cast<T*>(p.out) + (static_cast<int64_t>(query_row(p, s)) * p.hq + h0 + q) * D +
+             lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) dst[e] = from_float<T>(acc[q][e] * inv);
   }
-  const float inv = poisoned ? 0.f : 1.f / l;
-  T* dst = static_cast<T*>(p.out) + (static_cast<int64_t>(query_row(p, s)) * p.hq + h) * D + lane * kPer;
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) dst[e] = from_float<T>(acc[e] * inv);
 }
 
 template <typename T, int D, int G, int WH>
@@ -1636,8 +1664,12 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   // merge kernel, launched with programmatic stream serialization so its
   // launch overlaps the decode kernel's tail (it waits with griddepcontrol.wait);
   // launched on its own (after a join of streams) it needs no such overlap
+  // one warp per (sequence, head) while the rows fit in one wave of warps
+  // (64 per SM), else per (sequence, 4 heads)
+  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+  const int hpw = (a.num_q_heads % 4 == 0 && rows > 64LL * device_sm_count()) ? 4 : 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.num_seqs * a.num_q_heads + 7) / 8);
+  cfg.gridDim = dim3(static_cast<unsigned>((rows / hpw + 7) / 8));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -1646,7 +1678,8 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.launch_part == 2 ? 0 : 1;
-  return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<T, D>, p, grid);
+  if (hpw == 4) return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<T, D, 4>, p, grid);
+  return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<T, D, 1>, p, grid);
 }
 
 template <typename T, int D, int G>
