@@ -114,31 +114,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return mbar_wait_bounded_ns(bar, parity, kWaitLimitNs);
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// The same wait polling with test_wait (the thread never suspends): for a
-// thread whose next instruction after the wait is latency-critical.
-__device__ __forceinline__ bool mbar_poll_bounded(uint64_t* bar, uint32_t parity) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
 // 1-D bulk copy global -> shared, completing `bytes` on `bar`. Both addresses
 // 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
