@@ -136,6 +136,14 @@ PA_API int pa_bm_block_table(const pa_block_manager* bm, int64_t seq, int32_t* o
 /* Reference count of a physical block (-1 if out of range). */
 PA_API int pa_bm_refcount(const pa_block_manager* bm, int32_t block);
 
+/* Tokens that the n sequences seqs[0..n-1] (a request's beams or sampled
+ * replies) share as a sibling group of pa_decode_cascade_nested: the leading
+ * blocks that are the same physical blocks in every one's table, whole pages
+ * within every one's context, times the block size. Returns that count (0
+ * when they share no page), or PA_EINVAL for n < 1, a null array or an
+ * unknown sequence. */
+PA_API int64_t pa_bm_shared_prefix(const pa_block_manager* bm, const int64_t* seqs, int n);
+
 /* A scheduler over bm: token_budget tokens per step, prefill chunks of at
  * most chunk_size tokens, at most max_running sequences. */
 PA_API pa_scheduler* pa_sched_create(pa_block_manager* bm, int token_budget, int chunk_size,

@@ -304,6 +304,28 @@ int pa_bm_refcount(const pa_block_manager* bm, int32_t block) {
   return bm->refcount[block];
 }
 
+int64_t pa_bm_shared_prefix(const pa_block_manager* bm, const int64_t* seqs, int n) {
+  if (bm == nullptr || seqs == nullptr || n < 1) return PA_EINVAL;
+  std::vector<const pa_block_manager::Seq*> members;
+  members.reserve(n);
+  int64_t pages = INT64_MAX;
+  for (int i = 0; i < n; ++i) {
+    auto it = bm->seqs.find(seqs[i]);
+    if (it == bm->seqs.end()) return PA_EINVAL;
+    members.push_back(&it->second);
+    // whole pages inside this member's context
+    pages = std::min(pages, it->second.tokens / bm->block_size);
+  }
+  int64_t j = 0;
+  for (; j < pages; ++j) {
+    const int32_t b = members[0]->blocks[j];
+    bool same = true;
+    for (int i = 1; i < n && same; ++i) same = members[i]->blocks[j] == b;
+    if (!same) break;
+  }
+  return j * bm->block_size;
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------------ scheduler

@@ -83,6 +83,8 @@ def _lib() -> ctypes.CDLL:
         lib.pa_bm_block_table.argtypes = [P, I64, P, I]
         lib.pa_bm_refcount.restype = I
         lib.pa_bm_refcount.argtypes = [P, ctypes.c_int32]
+        lib.pa_bm_shared_prefix.restype = ctypes.c_int64
+        lib.pa_bm_shared_prefix.argtypes = [P, P, I]
         lib.pa_sched_create.restype = P
         lib.pa_sched_create.argtypes = [P, I, I, I]
         lib.pa_sched_destroy.restype = None
@@ -182,6 +184,15 @@ class BlockManager:
         if n < 0:
             raise abi.PagedAttentionError("pa_bm_block_table", n)
         return out[:n].copy()
+
+    def shared_prefix(self, seqs) -> int:
+        """Tokens the sequences share as a sibling group (whole pages that are
+        the same physical blocks in every table, within every context)."""
+        ids = np.ascontiguousarray(np.asarray(seqs, dtype=np.int64))
+        n = int(self._lib.pa_bm_shared_prefix(self._h, _np_ptr(ids), int(ids.size)))
+        if n < 0:
+            abi._check("pa_bm_shared_prefix", n)
+        return n
 
     def refcount(self, block: int) -> int:
         return int(self._lib.pa_bm_refcount(self._h, block))

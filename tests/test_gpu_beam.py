@@ -177,6 +177,8 @@ def test_beam_search_nested_cascade_decode(B):
             tables[i, :len(t)] = torch.from_numpy(t)
         lens = [sibling_shared_tokens(tables[r * B:(r + 1) * B].numpy(), ctx[r * B:(r + 1) * B])
                 for r in range(R)]
+        # the native block manager's answer from its own tables
+        assert lens == [bm.shared_prefix(order[r * B:(r + 1) * B]) for r in range(R)]
         shared_seen += sum(lens)
         q = torch.randn(S, hq, d, generator=g).to(dtype)
         out = torch.empty(S, hq, d, dtype=dtype, device="cuda")

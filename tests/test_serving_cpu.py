@@ -220,3 +220,14 @@ def test_sibling_shared_tokens_on_beams():
     assert n == 64
     assert all(bm.refcount(int(rows[0][j])) == 3 for j in range(n // 16))
     assert bm.refcount(int(rows[0][4])) == 1
+    # the native block manager gives the same count
+    assert bm.shared_prefix([1, 2, 3]) == 64 == bm.shared_prefix([3, 1])
+    assert bm.shared_prefix([2]) == 64                 # one member: its whole pages (71 tokens)
+    for b in (1, 2):
+        bm.append(b, 60)                             # 131 tokens: pages 4..7 private
+    assert bm.shared_prefix([1, 2, 3]) == 64
+    assert bm.shared_prefix([1]) == 128
+    with pytest.raises(abi.PagedAttentionError):
+        bm.shared_prefix([1, 99])                    # unknown sequence
+    with pytest.raises(abi.PagedAttentionError):
+        bm.shared_prefix([])
